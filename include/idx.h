@@ -1,0 +1,157 @@
+/*
+ * idx.h - C ABI of the GB300 decode indexer library (libidx.so).
+ *
+ * The indexer of the sglang PR 48224 page (sgl-amd-mono #86, "... first digits
+ * from the scoring"): for every decode row it "scores every cached key of each
+ * row and then selects each row's exact top-2048" (section Motivation, first
+ * paragraph), reading an FP8 E4M3 or bf16 paged key cache (section Accuracy
+ * Tests), dropping "keys at or past a row's bound" (section Modifications,
+ * commit 2), and selecting by radix digits whose first digit is radix_key >> 26
+ * over 64 bins (section Modifications, commit 4).  The score of the key at
+ * logical position t for row r is
+ *
+ *     score[r][t] = sum_{h<64} w[r][h] * ReLU(scale_t * <q[r][h][:], k_t>)
+ *
+ * with 64 heads of 128 dimensions; scale_t is the key's fp32 scale (E4M3 cache)
+ * or 1 (bf16 cache).
+ *
+ * Conventions for every call below:
+ *   - Pointers named "device" are caller-owned device memory; the library never
+ *     allocates, frees or keeps them.  Pointers named "host" are host memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     is asynchronous on it unless its comment says otherwise.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns IDX_EINVAL (or IDX_EUNSUPPORTED for a shape the library
+ *     does not handle) and launches nothing.  A failed launch returns IDX_ECUDA.
+ *   - Errors found on the device (a page id outside [0, P), a row bound above
+ *     pt_stride * 64, a pipeline wait that ran out of time) never trap: the kernel
+ *     records them in a status word inside the workspace and finishes; read it
+ *     with idx_last_device_status().
+ *   - Key positions are logical positions within the row's request: position t
+ *     lives in physical page page_table[req * pt_stride + t / 64], slot t % 64.
+ */
+#ifndef IDX_H
+#define IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IDX_HEADS 64      /* query heads per row */
+#define IDX_DIM 128       /* dimensions per head and per key */
+#define IDX_PAGE 64       /* tokens per cache page */
+#define IDX_MAX_K 2048    /* largest top-k */
+#define IDX_MAX_ROWS 65535
+
+typedef enum {
+    IDX_OK = 0,
+    IDX_EINVAL = 1,       /* bad argument (null pointer, negative size, small workspace ...) */
+    IDX_EUNSUPPORTED = 2, /* valid but outside what this build handles */
+    IDX_ECUDA = 3,        /* a CUDA runtime call or launch failed */
+    IDX_ETIMEOUT = 4,     /* a device-side wait ran out of time (device status only) */
+    IDX_EDEVICE = 5       /* bad data seen on the device: page id or bound out of range */
+} idx_status;
+
+typedef enum {
+    IDX_KV_E4M3 = 0,      /* keys are OCP E4M3 bytes with one fp32 scale per token */
+    IDX_KV_BF16 = 1       /* keys are bf16, scale 1 */
+} idx_kv_dtype;
+
+/* One indexer problem.  All array pointers are device memory owned by the caller. */
+typedef struct {
+    const void *q;             /* bf16 [R][64][128], contiguous, 16-byte aligned */
+    const float *w;            /* fp32 [R][64], contiguous, 16-byte aligned */
+    const void *k_cache;       /* [P][64][128]: E4M3 bytes or bf16, contiguous, 16-byte aligned */
+    const float *k_scale;      /* fp32 [P][64] for IDX_KV_E4M3, 16-byte aligned, every value >= 0;
+                                  must be NULL for IDX_KV_BF16 */
+    const int32_t *page_table; /* int32 [Q][pt_stride]: page ids in [0, P) for every page a row reads */
+    const int32_t *row_req;    /* int32 [R]: request of each row, in [0, Q) */
+    const int32_t *row_bound;  /* int32 [R]: row r scores positions 0 .. row_bound[r]-1 */
+    int32_t R;                 /* rows, 1 .. IDX_MAX_ROWS */
+    int32_t Q;                 /* requests, >= 1 */
+    int64_t P;                 /* pages in the cache, >= 1 */
+    int32_t pt_stride;         /* page-table row length, >= 1 */
+    int32_t max_bound;         /* host upper bound on every row_bound[r]; sizes scratch, so no
+                                  device-to-host read is needed; 0 <= max_bound <= pt_stride*64 */
+    int32_t kv_dtype;          /* idx_kv_dtype */
+} idx_problem;
+
+/* Bytes of device workspace that idx_score / idx_topk / idx_launch need for this
+ * problem and top-k (the largest of the three; every call accepts more).  The
+ * workspace is caller-owned, needs no initialisation and may be reused by later
+ * calls on the same stream; two calls that overlap in time need two workspaces.
+ * Returns 0 if the problem is invalid. */
+size_t idx_workspace_size(const idx_problem *problem, int32_t K);
+
+/* Scores only (the scan and contraction; section Motivation, first paragraph).
+ *   scores  device fp32 [R][ld], ld >= max_bound: scores[r][t] written for t < row_bound[r],
+ *           other entries untouched.
+ *   hist    device uint32 [R][64] or NULL: when given, hist[r][d] = number of t < row_bound[r]
+ *           with radix_key(scores[r][t]) >> 26 == d (the fused first-digit histogram of
+ *           section Modifications, commit 4).  radix_key maps the fp32 bits to an unsigned key
+ *           that orders like the value, with -0.0 read as +0.0.
+ *   ws      device workspace of ws_bytes >= idx_workspace_size(problem, 1). */
+idx_status idx_score(const idx_problem *problem, float *scores, int64_t ld, uint32_t *hist,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* Exact top-K of given scores (section Motivation: exact top-2048; section
+ * Modifications, commit 4: radix selection with a 64-bin first digit).
+ *   scores     device fp32 [R][ld]; only t < row_bound[r] is read; values must not be NaN.
+ *   row_bound  device int32 [R]; max_bound (host) >= every row_bound[r], ld >= max_bound.
+ *   K          1 .. IDX_MAX_K.
+ *   hist       device uint32 [R][64] first-digit histogram of these scores (as idx_score
+ *              writes it) or NULL, in which case it is computed here.
+ *   out_idx    device int32 [R][K]: positions ordered by score descending, then position
+ *              ascending; entries past min(K, row_bound[r]) are -1.  Scores compare by value
+ *              (-0.0 == +0.0).
+ *   ws         device workspace of ws_bytes >= idx_workspace_size() of a problem with these
+ *              R and max_bound. */
+idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R,
+                    int32_t max_bound, int32_t K, const uint32_t *hist, int32_t *out_idx,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/* The fused indexer launch: idx_score into workspace scratch, the fused first-digit
+ * histogram, then idx_topk; out_idx as for idx_topk. */
+idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* Bytes of device arena idx_launch_host needs: the inputs' device copies, the
+ * output and the workspace. */
+size_t idx_host_arena_size(const idx_problem *host_problem, int32_t K);
+
+/* idx_launch on HOST inputs.  host_problem's array pointers are host memory (pinned
+ * memory makes the copies asynchronous; pageable memory makes them synchronous).
+ * Copies every input into `arena` (device, arena_bytes >= idx_host_arena_size()),
+ * runs idx_launch and copies the [R][K] result back into host_out (host).  All
+ * copies are issued on `stream`; the caller synchronises the stream before reading
+ * host_out. */
+idx_status idx_launch_host(const idx_problem *host_problem, int32_t K, int32_t *host_out,
+                           void *arena, size_t arena_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of workspace
+ * `ws` (of the last call that used it): IDX_OK, IDX_ETIMEOUT or IDX_EDEVICE, or
+ * IDX_ECUDA if the stream reports an error. */
+idx_status idx_last_device_status(void *ws, void *stream);
+
+/* Static description of a status code. */
+const char *idx_status_string(idx_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t idx_version(void);
+
+/* Test hooks.  IDX_DEBUG_WAIT_LIMIT_NS sets the time limit of every device-side wait
+ * (default 1e9 ns); IDX_DEBUG_STALL_SCORE_MMA > 0 makes the next scoring launch hold
+ * back its first accumulator hand-off, so that its waits run out and it reports
+ * IDX_ETIMEOUT.  Process-wide; returns the previous value.  Not for production use. */
+#define IDX_DEBUG_WAIT_LIMIT_NS 1
+#define IDX_DEBUG_STALL_SCORE_MMA 2
+int64_t idx_debug_set(int32_t what, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H */

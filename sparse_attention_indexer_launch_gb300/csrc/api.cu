@@ -1,0 +1,387 @@
+// The C ABI (include/idx.h): argument checks, workspace carving, the key
+// cache's TMA descriptor, and the order of launches on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "idx.h"
+#include "idx_device.cuh"
+#include "launch.h"
+
+namespace {
+
+using idx::Workspace;
+
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t g_wait_limit_ns = 1000000000LL;
+int64_t g_stall_next = 0;
+std::mutex g_mu;
+
+struct Layout {
+  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist1, hist2, rowsel, win, tie, scores;
+  size_t total;
+  int64_t scores_ld;
+};
+
+Layout make_layout(int64_t R, int64_t K, int64_t max_bound, bool with_scores) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kAlign);
+    return at;
+  };
+  L.status = take(256);
+  L.plan = take(sizeof(idx::PlanHeader));
+  L.groups = take(static_cast<size_t>(R) * sizeof(idx::Group));
+  L.bound_eff = take(static_cast<size_t>(R) * 4);
+  L.qop0 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
+  L.qop1 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
+  L.wq = take(static_cast<size_t>(R) * idx::kHeads * 4);
+  L.hist1 = take(static_cast<size_t>(R) * 64 * 4);
+  L.hist2 = take(static_cast<size_t>(R) * 4096 * 4);
+  L.rowsel = take(static_cast<size_t>(R) * sizeof(idx::RowSelect));
+  L.win = take(static_cast<size_t>(R) * K * 8);
+  L.tie = take(static_cast<size_t>(R) * idx::kTieCap * 8);
+  L.scores_ld = static_cast<int64_t>(align_up(static_cast<size_t>(max_bound > 0 ? max_bound : 1), 4));
+  L.scores = take(with_scores ? static_cast<size_t>(R) * L.scores_ld * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+Workspace carve(void *base, const Layout &L) {
+  uint8_t *b = static_cast<uint8_t *>(base);
+  Workspace w{};
+  w.status = reinterpret_cast<uint32_t *>(b + L.status);
+  w.plan = reinterpret_cast<idx::PlanHeader *>(b + L.plan);
+  w.groups = reinterpret_cast<idx::Group *>(b + L.groups);
+  w.bound_eff = reinterpret_cast<int32_t *>(b + L.bound_eff);
+  w.qop0 = b + L.qop0;
+  w.qop1 = b + L.qop1;
+  w.wq = reinterpret_cast<float *>(b + L.wq);
+  w.hist1 = reinterpret_cast<uint32_t *>(b + L.hist1);
+  w.hist2 = reinterpret_cast<uint32_t *>(b + L.hist2);
+  w.rowsel = reinterpret_cast<idx::RowSelect *>(b + L.rowsel);
+  w.win = reinterpret_cast<unsigned long long *>(b + L.win);
+  w.tie = reinterpret_cast<unsigned long long *>(b + L.tie);
+  w.scores = reinterpret_cast<float *>(b + L.scores);
+  w.scores_ld = L.scores_ld;
+  return w;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+idx_status check_problem(const idx_problem *p) {
+  if (p == nullptr) return IDX_EINVAL;
+  if (p->q == nullptr || p->w == nullptr || p->k_cache == nullptr || p->page_table == nullptr ||
+      p->row_req == nullptr || p->row_bound == nullptr)
+    return IDX_EINVAL;
+  if (p->R < 1 || p->Q < 1 || p->P < 1 || p->pt_stride < 1 || p->max_bound < 0) return IDX_EINVAL;
+  if (p->R > IDX_MAX_ROWS) return IDX_EUNSUPPORTED;
+  if (static_cast<int64_t>(p->max_bound) > static_cast<int64_t>(p->pt_stride) * IDX_PAGE) return IDX_EINVAL;
+  if (p->P > (INT32_MAX / IDX_PAGE)) return IDX_EUNSUPPORTED;  // TMA row coordinate is 32-bit
+  if (p->kv_dtype == IDX_KV_E4M3) {
+    if (p->k_scale == nullptr || !aligned16(p->k_scale)) return IDX_EINVAL;
+  } else if (p->kv_dtype == IDX_KV_BF16) {
+    if (p->k_scale != nullptr) return IDX_EINVAL;
+  } else {
+    return IDX_EINVAL;
+  }
+  if (!aligned16(p->q) || !aligned16(p->w) || !aligned16(p->k_cache)) return IDX_EINVAL;
+  return IDX_OK;
+}
+
+// ---------------------------------------------------------------------------- device info
+int g_num_sms[128];
+
+idx_status device_sms(int *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ECUDA;
+  if (dev < 0 || dev >= 128) return IDX_EUNSUPPORTED;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IDX_ECUDA;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return IDX_EUNSUPPORTED;  // built for sm_103a only
+    g_num_sms[dev] = n;
+  }
+  *out = g_num_sms[dev];
+  return IDX_OK;
+}
+
+// ---------------------------------------------------------------------------- TMA descriptor
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+idx_status key_tensor_map(const idx_problem *p, CUtensorMap *map) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return IDX_ECUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const bool f8 = p->kv_dtype == IDX_KV_E4M3;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(IDX_DIM), static_cast<cuuint64_t>(p->P) * IDX_PAGE};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(f8 ? IDX_DIM : IDX_DIM * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(f8 ? 128 : 64), static_cast<cuuint32_t>(IDX_PAGE)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void *>(p->k_cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IDX_OK : IDX_ECUDA;
+}
+
+idx_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? IDX_OK : IDX_ECUDA; }
+
+// prep + scoring launches shared by idx_score and idx_launch.
+idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, int64_t ld, uint32_t *hist,
+                       bool clear_select, cudaStream_t s) {
+  int sms = 0;
+  idx_status st = device_sms(&sms);
+  if (st != IDX_OK) return st;
+  CUtensorMap map;
+  st = key_tensor_map(p, &map);
+  if (st != IDX_OK) return st;
+  idx::PrepArgs pa{};
+  pa.q = p->q;
+  pa.w = p->w;
+  pa.row_req = p->row_req;
+  pa.row_bound = p->row_bound;
+  pa.R = p->R;
+  pa.Q = p->Q;
+  pa.pt_stride = p->pt_stride;
+  pa.max_bound = p->max_bound;
+  pa.kv_dtype = p->kv_dtype;
+  pa.hist_target = hist;
+  pa.clear_select = clear_select ? 1 : 0;
+  pa.ws = w;
+  st = cuda_ok(idx::launch_prep(pa, s));
+  if (st != IDX_OK) return st;
+  idx::ScoreArgs sa{};
+  sa.page_table = p->page_table;
+  sa.k_scale = p->k_scale;
+  sa.P = p->P;
+  sa.pt_stride = p->pt_stride;
+  sa.scores = scores;
+  sa.ld = ld;
+  sa.hist = hist;
+  sa.ws = w;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    sa.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns);
+    sa.stall_first_handoff = g_stall_next > 0 ? 1 : 0;
+    if (g_stall_next > 0) --g_stall_next;
+  }
+  return cuda_ok(idx::launch_score(map, sa, p->kv_dtype, sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t idx_workspace_size(const idx_problem *problem, int32_t K) {
+  if (check_problem(problem) != IDX_OK || K < 1 || K > IDX_MAX_K) return 0;
+  return make_layout(problem->R, K, problem->max_bound, true).total;
+}
+
+idx_status idx_score(const idx_problem *problem, float *scores, int64_t ld, uint32_t *hist, void *ws,
+                     size_t ws_bytes, void *stream) {
+  idx_status st = check_problem(problem);
+  if (st != IDX_OK) return st;
+  if (scores == nullptr || ws == nullptr || ld < 1 || ld < problem->max_bound) return IDX_EINVAL;
+  const Layout L = make_layout(problem->R, 1, problem->max_bound, false);
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
+  const Workspace w = carve(ws, L);
+  return run_scoring(problem, w, scores, ld, hist != nullptr ? hist : w.hist1, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R, int32_t max_bound,
+                    int32_t K, const uint32_t *hist, int32_t *out_idx, void *ws, size_t ws_bytes, void *stream) {
+  if (scores == nullptr || row_bound == nullptr || out_idx == nullptr || ws == nullptr) return IDX_EINVAL;
+  if (R < 1 || max_bound < 0 || K < 1 || K > IDX_MAX_K || ld < 1 || ld < max_bound) return IDX_EINVAL;
+  if (R > IDX_MAX_ROWS) return IDX_EUNSUPPORTED;
+  const Layout L = make_layout(R, K, max_bound, false);
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
+  int sms = 0;
+  idx_status st = device_sms(&sms);
+  if (st != IDX_OK) return st;
+  const Workspace w = carve(ws, L);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_ok(cudaMemsetAsync(w.status, 0, 4, s));
+  if (st != IDX_OK) return st;
+  idx::SelectArgs a{};
+  a.scores = scores;
+  a.ld = ld;
+  a.bound = w.bound_eff;
+  a.R = R;
+  a.K = K;
+  a.max_bound = max_bound;
+  a.hist1 = hist != nullptr ? hist : w.hist1;
+  a.out_idx = out_idx;
+  a.ws = w;
+  st = cuda_ok(idx::launch_select_clear(a, row_bound, hist != nullptr ? nullptr : w.hist1, s));
+  if (st != IDX_OK) return st;
+  if (hist == nullptr) {
+    st = cuda_ok(idx::launch_first_hist(a, w.hist1, s));
+    if (st != IDX_OK) return st;
+  }
+  return cuda_ok(idx::launch_select(a, s));
+}
+
+idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws, size_t ws_bytes,
+                      void *stream) {
+  idx_status st = check_problem(problem);
+  if (st != IDX_OK) return st;
+  if (out_idx == nullptr || ws == nullptr || K < 1 || K > IDX_MAX_K) return IDX_EINVAL;
+  const Layout L = make_layout(problem->R, K, problem->max_bound, true);
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
+  const Workspace w = carve(ws, L);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_scoring(problem, w, w.scores, w.scores_ld, w.hist1, true, s);
+  if (st != IDX_OK) return st;
+  idx::SelectArgs a{};
+  a.scores = w.scores;
+  a.ld = w.scores_ld;
+  a.bound = w.bound_eff;
+  a.R = problem->R;
+  a.K = K;
+  a.max_bound = problem->max_bound;
+  a.hist1 = w.hist1;
+  a.out_idx = out_idx;
+  a.ws = w;
+  return cuda_ok(idx::launch_select(a, s));
+}
+
+// ---------------------------------------------------------------------------- host inputs
+namespace {
+struct HostArena {
+  size_t q, w, kc, ks, pt, rr, rb, out, ws, total;
+};
+
+HostArena host_arena(const idx_problem *p, int32_t K) {
+  HostArena A{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kAlign);
+    return at;
+  };
+  const size_t key_bytes = static_cast<size_t>(p->P) * IDX_PAGE * IDX_DIM * (p->kv_dtype == IDX_KV_E4M3 ? 1 : 2);
+  A.q = take(static_cast<size_t>(p->R) * IDX_HEADS * IDX_DIM * 2);
+  A.w = take(static_cast<size_t>(p->R) * IDX_HEADS * 4);
+  A.kc = take(key_bytes);
+  A.ks = take(p->kv_dtype == IDX_KV_E4M3 ? static_cast<size_t>(p->P) * IDX_PAGE * 4 : 0);
+  A.pt = take(static_cast<size_t>(p->Q) * p->pt_stride * 4);
+  A.rr = take(static_cast<size_t>(p->R) * 4);
+  A.rb = take(static_cast<size_t>(p->R) * 4);
+  A.out = take(static_cast<size_t>(p->R) * K * 4);
+  A.ws = take(make_layout(p->R, K, p->max_bound, true).total);
+  A.total = off;
+  return A;
+}
+}  // namespace
+
+size_t idx_host_arena_size(const idx_problem *host_problem, int32_t K) {
+  if (check_problem(host_problem) != IDX_OK || K < 1 || K > IDX_MAX_K) return 0;
+  return host_arena(host_problem, K).total;
+}
+
+idx_status idx_launch_host(const idx_problem *hp, int32_t K, int32_t *host_out, void *arena, size_t arena_bytes,
+                           void *stream) {
+  idx_status st = check_problem(hp);
+  if (st != IDX_OK) return st;
+  if (host_out == nullptr || arena == nullptr || K < 1 || K > IDX_MAX_K) return IDX_EINVAL;
+  const HostArena A = host_arena(hp, K);
+  if (arena_bytes < A.total || (reinterpret_cast<uintptr_t>(arena) & (kAlign - 1)) != 0) return IDX_EINVAL;
+  uint8_t *b = static_cast<uint8_t *>(arena);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f8 = hp->kv_dtype == IDX_KV_E4M3;
+  struct Copy {
+    size_t off;
+    const void *src;
+    size_t bytes;
+  } copies[] = {
+      {A.q, hp->q, static_cast<size_t>(hp->R) * IDX_HEADS * IDX_DIM * 2},
+      {A.w, hp->w, static_cast<size_t>(hp->R) * IDX_HEADS * 4},
+      {A.kc, hp->k_cache, static_cast<size_t>(hp->P) * IDX_PAGE * IDX_DIM * (f8 ? 1 : 2)},
+      {A.ks, hp->k_scale, f8 ? static_cast<size_t>(hp->P) * IDX_PAGE * 4 : 0},
+      {A.pt, hp->page_table, static_cast<size_t>(hp->Q) * hp->pt_stride * 4},
+      {A.rr, hp->row_req, static_cast<size_t>(hp->R) * 4},
+      {A.rb, hp->row_bound, static_cast<size_t>(hp->R) * 4},
+  };
+  for (const Copy &c : copies) {
+    if (c.bytes == 0) continue;
+    st = cuda_ok(cudaMemcpyAsync(b + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, s));
+    if (st != IDX_OK) return st;
+  }
+  idx_problem dp = *hp;
+  dp.q = b + A.q;
+  dp.w = reinterpret_cast<const float *>(b + A.w);
+  dp.k_cache = b + A.kc;
+  dp.k_scale = f8 ? reinterpret_cast<const float *>(b + A.ks) : nullptr;
+  dp.page_table = reinterpret_cast<const int32_t *>(b + A.pt);
+  dp.row_req = reinterpret_cast<const int32_t *>(b + A.rr);
+  dp.row_bound = reinterpret_cast<const int32_t *>(b + A.rb);
+  int32_t *dout = reinterpret_cast<int32_t *>(b + A.out);
+  st = idx_launch(&dp, K, dout, b + A.ws, A.total - A.ws, stream);
+  if (st != IDX_OK) return st;
+  return cuda_ok(cudaMemcpyAsync(host_out, dout, static_cast<size_t>(hp->R) * K * 4, cudaMemcpyDeviceToHost, s));
+}
+
+idx_status idx_last_device_status(void *ws, void *stream) {
+  if (ws == nullptr) return IDX_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return IDX_ECUDA;
+  uint32_t word = 0;
+  uint32_t *status = static_cast<uint32_t *>(ws);  // the status word is the workspace's first word
+  if (cudaMemcpy(&word, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return IDX_ECUDA;
+  if (cudaMemset(status, 0, 4) != cudaSuccess) return IDX_ECUDA;
+  if (word & idx::kStatusTimeout) return IDX_ETIMEOUT;
+  if (word & (idx::kStatusBadPage | idx::kStatusBadBound)) return IDX_EDEVICE;
+  return IDX_OK;
+}
+
+const char *idx_status_string(idx_status status) {
+  switch (status) {
+    case IDX_OK: return "ok";
+    case IDX_EINVAL: return "invalid argument";
+    case IDX_EUNSUPPORTED: return "unsupported shape or device";
+    case IDX_ECUDA: return "CUDA error";
+    case IDX_ETIMEOUT: return "a device-side wait ran out of time";
+    case IDX_EDEVICE: return "out-of-range page id or row bound seen on the device";
+  }
+  return "unknown status";
+}
+
+int32_t idx_version(void) { return 100; }
+
+int64_t idx_debug_set(int32_t what, int64_t value) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int64_t prev = 0;
+  if (what == IDX_DEBUG_WAIT_LIMIT_NS) {
+    prev = g_wait_limit_ns;
+    g_wait_limit_ns = value > 0 ? value : 1000000000LL;
+  } else if (what == IDX_DEBUG_STALL_SCORE_MMA) {
+    prev = g_stall_next;
+    g_stall_next = value > 0 ? value : 0;
+  }
+  return prev;
+}
+
+}  // extern "C"

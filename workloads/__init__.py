@@ -107,16 +107,23 @@ def quantize_e4m3(x: np.ndarray):
     return np.ascontiguousarray(codes), scale
 
 
-def _draw_keys(rng: np.random.Generator, n: int, kv_dtype: str, key_dist: str):
-    chunk = 1 << 18
+def _draw_keys(seed: int, n: int, kv_dtype: str, key_dist: str):
+    """Keys in chunks of 2^16 tokens; chunk c draws from default_rng([seed, 7, c]) so
+    the result does not depend on how many threads fill the chunks."""
+    import concurrent.futures
+    import os
+    chunk = 1 << 16
     if kv_dtype == "e4m3":
         codes = np.empty((n, DIM), dtype=np.uint8)
         scales = np.empty(n, dtype=np.float32)
     else:
         codes = np.empty((n, DIM), dtype=np.uint16)
         scales = None
-    for s0 in range(0, n, chunk):
+
+    def fill(c):
+        s0 = c * chunk
         m = min(chunk, n - s0)
+        rng = np.random.default_rng([seed, 7, c])
         x = rng.standard_normal((m, DIM), dtype=np.float32)
         if key_dist == "mixture":
             sigma = np.where(rng.random(m) < 0.5, np.float32(1.0), np.float32(4.0)).astype(np.float32)
@@ -124,11 +131,16 @@ def _draw_keys(rng: np.random.Generator, n: int, kv_dtype: str, key_dist: str):
         elif key_dist != "normal":
             raise ValueError(key_dist)
         if kv_dtype == "e4m3":
-            c, sc = quantize_e4m3(x)
-            codes[s0:s0 + m] = c
+            cq, sc = quantize_e4m3(x)
+            codes[s0:s0 + m] = cq
             scales[s0:s0 + m] = sc
         else:
             codes[s0:s0 + m] = _bf16_bits(x)
+
+    nchunks = (n + chunk - 1) // chunk
+    workers = max(1, min(16, os.cpu_count() or 1, nchunks))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(fill, range(nchunks)))
     return codes, scales
 
 
@@ -156,7 +168,7 @@ def build(name: str, lengths, rows_per_req, kv_dtype: str = "e4m3", seed: int = 
     q = _bf16_bits(rng.standard_normal((R, HEADS, DIM), dtype=np.float32))
     w = (rng.standard_normal((R, HEADS), dtype=np.float32) / np.float32(8.0)).astype(np.float32)
 
-    codes, scales = _draw_keys(rng, P * PAGE, kv_dtype, key_dist)
+    codes, scales = _draw_keys(seed, P * PAGE, kv_dtype, key_dist)
     k_cache = codes.reshape(P, PAGE, DIM)
     k_scale = None if scales is None else scales.reshape(P, PAGE)
 
