@@ -1,0 +1,384 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused indexer launch (idx_launch) on GB300.
+
+Workload: two requests x four rows at 524,288 cached keys each, FP8 E4M3 cache
+(the 512K-key configuration the metric is quoted on), seeded synthetic inputs
+from workloads.make_config(3).  One step = one idx_launch: plan + query prep,
+the scoring scan with the fused first-digit histogram, and the exact top-2048
+selection of every row.
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every step a 256 MB
+buffer (twice the L2) is written so that no step finds the keys in L2; each step
+is timed on the launching stream with CUDA events around the launch alone, and
+the scoring kernel is timed the same way through the library's event hook.  The
+e2e figure times idx_launch_host: host->device copies of every input from
+pinned memory, the launch, and the device->host copy of the indices.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+batch of requests (the work shards by request with no exchange), the timed
+region is bracketed by a barrier and synchronisation on every rank, and the
+maximum time over ranks is reported: weak scaling.
+
+`--impl reference` times the CPU oracle (the slow reference implementation of
+the same method) on the host cores instead; rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per indexer launch and key·rows/s at 512K keys; % of HBM/FP8 roofline"
+WORKLOAD = ("cfg3: 2 requests x 4 rows, 524,288 keys each (page 64, shuffled pages), FP8 E4M3 cache "
+            "with per-token scale, sigma 1/4 mixture keys, bf16 q, fp32 w, top-k 2048")
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_LAUNCH = 5  # prep, score, hist2, collect, finish
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def profile_traffic(kernel_src: str):
+    """DRAM bytes per launch of the scoring kernel from the committed ncu summary,
+    or None if the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_cfg3.md")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("score.cu sha256[:16]") != sha:
+        return None
+    try:
+        return int(fields["dram bytes per launch"].replace(",", ""))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(prob, orc, budget_s: float = 20.0):
+    """The oracle (score + exact top-k) on a bounded sample of the workload: whole
+    rows of the first request, as many as fit the time budget (at least one)."""
+    import numpy as np
+    import workloads
+    rows = [r for r in range(prob.R) if prob.row_req[r] == 0]
+    # time one row on a slice first to size the sample
+    sub = workloads.Problem(name="sample", q=prob.q[rows[:1]], w=prob.w[rows[:1]], k_cache=prob.k_cache,
+                            k_scale=prob.k_scale, page_table=prob.page_table, row_req=prob.row_req[rows[:1]],
+                            row_bound=prob.row_bound[rows[:1]], kv_dtype=prob.kv_dtype, K=prob.K)
+    t0 = time.perf_counter()
+    s = orc.score(sub)
+    orc.topk(s.astype(np.float32), sub.row_bound, sub.K)
+    dt = time.perf_counter() - t0
+    done_rows, done_keys, total_t = 1, int(sub.row_bound.sum()), dt
+    n_more = max(0, min(len(rows) - 1, int((budget_s - dt) / max(dt, 1e-6))))
+    if n_more > 0:
+        sel = rows[1:1 + n_more]
+        sub2 = workloads.Problem(name="sample", q=prob.q[sel], w=prob.w[sel], k_cache=prob.k_cache,
+                                 k_scale=prob.k_scale, page_table=prob.page_table, row_req=prob.row_req[sel],
+                                 row_bound=prob.row_bound[sel], kv_dtype=prob.kv_dtype, K=prob.K)
+        t0 = time.perf_counter()
+        s = orc.score(sub2)
+        orc.topk(s.astype(np.float32), sub2.row_bound, sub2.K)
+        total_t += time.perf_counter() - t0
+        done_rows += n_more
+        done_keys += int(sub2.row_bound.sum())
+    return {"value": done_keys / total_t, "unit": "key·rows/s", "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(total_t, 3),
+            "sample": f"{done_rows} of {prob.R} rows of the workload (whole rows, {done_keys} key-rows): "
+                      "oracle scores in fp64 + exact top-2048 by sort"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads
+    orc = oracle.default()
+    prob = workloads.make_config(3)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(prob, orc, budget_s=2.0)
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(prob, orc, budget_s=args.ref_budget))
+    v = statistics.median(x["value"] for x in vals)
+    ms = prob.key_rows / v * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "key·rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": prob.R, "seq_len": prob.max_bound,
+                   "parallelism": "host cores (oracle)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": "key·rows/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": v, "unit": "key·rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="3", help="workload: 0..4 or 3a (default 3)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not os.environ.get("IDX_BENCH_ALLOW_SHORT"):
+        print("note: warm-up raised to 3 steps", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_indexer_launch_gb300 as lib
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = args.config if args.config == "3a" else int(args.config)
+    if world > 1 and rank > 0 and cfg == 3:
+        # each rank its own batch of two 512K-key requests
+        prob = workloads.build(workloads.CONFIG_NAMES[3], [524288, 524288], [4, 4], "e4m3",
+                               seed=3 + 1000 * rank, key_dist="mixture")
+    else:
+        prob = workloads.make_config(cfg)
+    dp = lib.DeviceProblem(prob)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None, sev=None):
+        flush.zero_()
+        if sev is not None:
+            lib.profile_next_score(sev[0], sev[1])
+        if ev is not None:
+            ev[0].record(stream)
+        dp.launch(out)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = dp.status()
+    if st != lib.IDX_OK:
+        raise SystemExit(f"device status after warm-up: {lib.status_string(st)}")
+
+    def events(n):
+        out = []
+        for _ in range(n):
+            pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for e in pair:
+                e.record(stream)   # creates the CUDA event, so the library can record it too
+            out.append(pair)
+        return out
+
+    evs = events(args.steps)
+    sevs = events(args.steps)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(evs[i], sevs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    st = dp.status()
+    if st != lib.IDX_OK:
+        raise SystemExit(f"device status after the timed steps: {lib.status_string(st)}")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    score_ms = [a.elapsed_time(b) for a, b in sevs]
+    ms = statistics.mean(step_ms)
+    score_mean_ms = statistics.mean(score_ms)
+
+    # end to end through idx_launch_host (pinned host inputs, copies in the timed region)
+    e2e_ms = None
+    h2d = d2h = 0
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(getattr(prob, k))).pin_memory()
+                for k in ("q", "w", "k_cache", "k_scale", "page_table", "row_req", "row_bound")
+                if getattr(prob, k) is not None}
+        kv = lib.IDX_KV_E4M3 if prob.kv_dtype == "e4m3" else lib.IDX_KV_BF16
+        hp = lib.make_problem(host["q"], host["w"], host["k_cache"], host.get("k_scale"), host["page_table"],
+                              host["row_req"], host["row_bound"], prob.max_bound, kv)
+        arena = lib.alloc_bytes(lib.host_arena_size(hp, prob.K))
+        hout = torch.empty((prob.R, prob.K), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = hout.numel() * hout.element_size()
+        for _ in range(3):
+            lib.idx_launch_host(hp, prob.K, hout, arena)
+        torch.cuda.synchronize()
+        if not np.array_equal(hout.numpy(), out.cpu().numpy()):
+            raise SystemExit("idx_launch_host result differs from idx_launch")
+        n_e2e = max(3, min(args.steps, 10))
+        e2e_ev = events(n_e2e)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for a, b in e2e_ev:
+            flush.zero_()
+            a.record(stream)
+            lib.idx_launch_host(hp, prob.K, hout, arena)
+            b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([ms, score_mean_ms, e2e_ms or 0.0], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, score_mean_ms, e2e_ms = float(t[0]), float(t[1]), (float(t[2]) or None)
+
+    key_rows_total = prob.key_rows * world
+    value = key_rows_total / (ms * 1e-3)
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    fp8_tf = 2.0 * bf16_tf     # FP8 dense = 2 x bf16 dense (nominal ratio)
+    key_bytes = prob.key_bytes
+    flops = prob.mma_flops
+    # The metric's roofline: max(key bytes / HBM, FP8 flops / FP8 peak).
+    t_hbm = key_bytes / (hbm_gbs * 1e9)
+    t_fp8 = flops / (fp8_tf * 1e12)
+    t_roof = max(t_hbm, t_fp8)
+    bound = "hbm" if t_hbm >= t_fp8 else "tensor"
+    score_s = score_mean_ms * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = key_bytes / score_s / 1e9, hbm_gbs, "GB/s"
+    else:
+        achieved, peak, unit = flops / score_s / 1e12, fp8_tf, "TFLOP/s"
+    traffic = profile_traffic(os.path.join(ROOT, "sparse_attention_indexer_launch_gb300", "csrc", "score.cu"))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "key·rows/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "us_per_launch": ms * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3 x (2-term e4m3 split of bf16 q), fp32 accumulate" if prob.kv_dtype == "e4m3" else "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD if cfg == 3 else workloads.CONFIG_NAMES[cfg],
+                       "global_batch": prob.R * world, "seq_len": prob.max_bound,
+                       "parallelism": f"replicas x{world} (independent requests per GPU)",
+                       "l2": "flushed before every step (256 MB write)"},
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "score_kernel (scan + contraction + head reduction + histogram)",
+                         "kernel_us": score_mean_ms * 1e3,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json; FP8 = 2 x bf16)",
+                         "algorithmic_bytes": key_bytes, "algorithmic_flops": flops,
+                         "launch_roofline_us": t_roof * 1e6,
+                         "launch_frac_of_roofline": t_roof / (ms * 1e-3),
+                         "tensor_frac_fp8": flops / score_s / 1e12 / fp8_tf,
+                         "tensor_frac_bf16_precision_matched": flops / score_s / 1e12 / bf16_tf},
+            "clocks": clocks.summary(),
+            "gpu_launches": KERNELS_PER_LAUNCH * args.steps,
+            "wall_s_timed_region": t_wall,
+        }
+        if e2e_ms is not None:
+            line["e2e"] = {"value": key_rows_total / (e2e_ms * 1e-3), "unit": "key·rows/s",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        if not args.no_cpu_baseline:
+            import oracle
+            line["cpu_baseline"] = cpu_baseline(prob, oracle.default())
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -150,6 +150,12 @@ int32_t idx_version(void);
 #define IDX_DEBUG_STALL_SCORE_MMA 2
 int64_t idx_debug_set(int32_t what, int64_t value);
 
+/* Measurement hook.  When `start` and `stop` (cudaEvent_t) are non-NULL, the next
+ * idx_score or idx_launch records `start` on its stream just before the scoring
+ * kernel and `stop` just after it, so the scoring kernel alone can be timed with
+ * cudaEventElapsedTime.  Applies to one call, then clears itself.  Process-wide. */
+void idx_profile_events(void *start, void *stop);
+
 #ifdef __cplusplus
 }
 #endif

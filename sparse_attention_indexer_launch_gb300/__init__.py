@@ -24,7 +24,7 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
-           "idx_debug_set"]
+           "idx_debug_set", "idx_profile_events"]
 
 
 class IdxError(RuntimeError):
@@ -71,6 +71,8 @@ def _load():
     lib.idx_version.restype = i32
     lib.idx_debug_set.argtypes = [i32, i64]
     lib.idx_debug_set.restype = i64
+    lib.idx_profile_events.argtypes = [vp, vp]
+    lib.idx_profile_events.restype = None
     return lib
 
 
@@ -142,6 +144,11 @@ def idx_launch_host(host_problem: Problem, K: int, host_out, arena, stream=None)
 
 def last_device_status(ws, stream=None) -> int:
     return int(lib.idx_last_device_status(_ptr(ws), _stream(stream)))
+
+
+def profile_next_score(start_event, stop_event):
+    """Time the next scoring kernel with two torch.cuda.Event(enable_timing=True)."""
+    lib.idx_profile_events(ctypes.c_void_p(start_event.cuda_event), ctypes.c_void_p(stop_event.cuda_event))
 
 
 def version() -> int:

@@ -22,6 +22,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int64_t g_wait_limit_ns = 1000000000LL;
 int64_t g_stall_next = 0;
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 std::mutex g_mu;
 
 struct Layout {
@@ -181,13 +182,21 @@ idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, 
   sa.ld = ld;
   sa.hist = hist;
   sa.ws = w;
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     sa.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns);
     sa.stall_first_handoff = g_stall_next > 0 ? 1 : 0;
     if (g_stall_next > 0) --g_stall_next;
+    ev0 = g_prof_start;
+    ev1 = g_prof_stop;
+    g_prof_start = g_prof_stop = nullptr;
   }
-  return cuda_ok(idx::launch_score(map, sa, p->kv_dtype, sms, s));
+  if (ev0 != nullptr && cudaEventRecord(ev0, s) != cudaSuccess) return IDX_ECUDA;
+  st = cuda_ok(idx::launch_score(map, sa, p->kv_dtype, sms, s));
+  if (st != IDX_OK) return st;
+  if (ev1 != nullptr && cudaEventRecord(ev1, s) != cudaSuccess) return IDX_ECUDA;
+  return IDX_OK;
 }
 
 }  // namespace
@@ -370,6 +379,12 @@ const char *idx_status_string(idx_status status) {
 }
 
 int32_t idx_version(void) { return 100; }
+
+void idx_profile_events(void *start, void *stop) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
 
 int64_t idx_debug_set(int32_t what, int64_t value) {
   std::lock_guard<std::mutex> lk(g_mu);

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def idxlib():
-    from sparse_attention_indexer_launch_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sparse_attention_indexer_launch_gb300 as lib
     return lib
 
