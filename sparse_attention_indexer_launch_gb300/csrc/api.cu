@@ -26,7 +26,7 @@ cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 std::mutex g_mu;
 
 struct Layout {
-  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist1, hist2, rowsel, win, tie, scores;
+  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, rowsel, win, tie, scores;
   size_t total;
   int64_t scores_ld;
 };
@@ -46,8 +46,7 @@ Layout make_layout(int64_t R, int64_t K, int64_t max_bound, bool with_scores) {
   L.qop0 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
   L.qop1 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
   L.wq = take(static_cast<size_t>(R) * idx::kHeads * 4);
-  L.hist1 = take(static_cast<size_t>(R) * 64 * 4);
-  L.hist2 = take(static_cast<size_t>(R) * 4096 * 4);
+  L.hist12 = take(static_cast<size_t>(R) * idx::kHistBins * 4);
   L.rowsel = take(static_cast<size_t>(R) * sizeof(idx::RowSelect));
   L.win = take(static_cast<size_t>(R) * K * 8);
   L.tie = take(static_cast<size_t>(R) * idx::kTieCap * 8);
@@ -67,8 +66,7 @@ Workspace carve(void *base, const Layout &L) {
   w.qop0 = b + L.qop0;
   w.qop1 = b + L.qop1;
   w.wq = reinterpret_cast<float *>(b + L.wq);
-  w.hist1 = reinterpret_cast<uint32_t *>(b + L.hist1);
-  w.hist2 = reinterpret_cast<uint32_t *>(b + L.hist2);
+  w.hist12 = reinterpret_cast<uint32_t *>(b + L.hist12);
   w.rowsel = reinterpret_cast<idx::RowSelect *>(b + L.rowsel);
   w.win = reinterpret_cast<unsigned long long *>(b + L.win);
   w.tie = reinterpret_cast<unsigned long long *>(b + L.tie);
@@ -216,8 +214,7 @@ idx_status idx_score(const idx_problem *problem, float *scores, int64_t ld, uint
   const Layout L = make_layout(problem->R, 1, problem->max_bound, false);
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
   const Workspace w = carve(ws, L);
-  return run_scoring(problem, w, scores, ld, hist != nullptr ? hist : w.hist1, false,
-                     static_cast<cudaStream_t>(stream));
+  return run_scoring(problem, w, scores, ld, hist, false, static_cast<cudaStream_t>(stream));
 }
 
 idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R, int32_t max_bound,
@@ -241,16 +238,13 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
   a.R = R;
   a.K = K;
   a.max_bound = max_bound;
-  a.hist1 = hist != nullptr ? hist : w.hist1;
   a.out_idx = out_idx;
   a.ws = w;
-  st = cuda_ok(idx::launch_select_clear(a, row_bound, hist != nullptr ? nullptr : w.hist1, s));
+  st = cuda_ok(idx::launch_select_clear(a, row_bound, s));
   if (st != IDX_OK) return st;
-  if (hist == nullptr) {
-    st = cuda_ok(idx::launch_first_hist(a, w.hist1, s));
-    if (st != IDX_OK) return st;
-  }
-  return cuda_ok(idx::launch_select(a, s));
+  st = cuda_ok(idx::launch_hist12(a, hist, s));
+  if (st != IDX_OK) return st;
+  return cuda_ok(idx::launch_collect(a, s));
 }
 
 idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws, size_t ws_bytes,
@@ -262,7 +256,7 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
   const Workspace w = carve(ws, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_scoring(problem, w, w.scores, w.scores_ld, w.hist1, true, s);
+  st = run_scoring(problem, w, w.scores, w.scores_ld, nullptr, true, s);
   if (st != IDX_OK) return st;
   idx::SelectArgs a{};
   a.scores = w.scores;
@@ -271,10 +265,9 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   a.R = problem->R;
   a.K = K;
   a.max_bound = problem->max_bound;
-  a.hist1 = w.hist1;
   a.out_idx = out_idx;
   a.ws = w;
-  return cuda_ok(idx::launch_select(a, s));
+  return cuda_ok(idx::launch_collect(a, s));
 }
 
 // ---------------------------------------------------------------------------- host inputs

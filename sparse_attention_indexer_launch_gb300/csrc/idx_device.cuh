@@ -42,14 +42,16 @@ struct PlanHeader {
 };
 
 struct RowSelect {       // per-row selection state
-  uint32_t prefix;       // radix-key prefix (first 18 bits) that holds the k-th key
-  uint32_t above;        // keys whose prefix is strictly greater
-  uint32_t mode;         // 0 = nothing to select (bound <= K: take all), 1 = threshold known
-  uint32_t nslices_done; // arrivals of the histogram kernel's slices
-  uint32_t win_count;    // winners appended by the collect kernel
-  uint32_t tie_count;    // threshold-bin candidates appended by the collect kernel
-  uint32_t pad[2];
+  uint32_t nslices_done; // arrivals of the collect kernel's slices
+  uint32_t win_count;    // keys above the threshold bin, appended by the collect kernel
+  uint32_t tie_count;    // keys in the threshold bin, appended by the collect kernel
+  uint32_t pad[5];
 };
+
+// The fused score histogram counts the top kHistBits bits of radix_key(score):
+// its 64-bin marginal (top 6 bits) is the first digit radix_key >> 26.
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;
 
 struct Workspace {
   uint32_t *status;        // [1]
@@ -58,17 +60,16 @@ struct Workspace {
   int32_t *bound_eff;      // [R]       row bounds after the device-side range check
   uint8_t *qop0;           // [R][8192]  FP8: q_hi; bf16: dims 0..63   (MMA B operand, swizzled)
   uint8_t *qop1;           // [R][8192]  FP8: q_lo; bf16: dims 64..127
-  float *wq;               // [R][64]    weights with the query prescale folded in
-  uint32_t *hist1;         // [R][64]    first-digit histogram (internal copy)
-  uint32_t *hist2;         // [R][4096]  second-digit histogram
+  float *wq;               // [R][64]    weights / 2 with the query prescale folded in
+  uint32_t *hist12;        // [R][4096]  12-bit histogram of the radix keys
   RowSelect *rowsel;       // [R]
-  unsigned long long *win; // [R][K]     winners (composite keys)
-  unsigned long long *tie; // [R][kTieCap] threshold-bin candidates
+  unsigned long long *win; // [R][K]     keys above the threshold bin (composite keys)
+  unsigned long long *tie; // [R][kTieCap] keys in the threshold bin
   float *scores;           // [R][ld]    score scratch of idx_launch (else unused)
   int64_t scores_ld;
 };
 
-constexpr int kTieCap = 4096;
+constexpr int kTieCap = 8192;
 
 // ---------------------------------------------------------------------------- timing
 __device__ __forceinline__ uint64_t global_ns() {
@@ -115,19 +116,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware up to `hint_ns` while the
+// phase is incomplete, instead of spinning on the issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` nanoseconds, or at once if *abort is set by another role of the CTA;
+// `limit_ns` nanoseconds, or once *abort is set by another role of the CTA;
 // returns false then (the caller records the timeout and unwinds).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (global_ns() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -155,6 +168,16 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
           smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Programmatic dependent launch: wait until the grid this launch depends on has
+// completed and its memory is visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the dependent grid be scheduled once every CTA of this grid has called it.
+__device__ __forceinline__ void grid_dependency_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
@@ -238,6 +261,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 32 lanes x 64 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+        "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+        "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -247,6 +291,10 @@ __device__ __forceinline__ void tmem_wait_ld() {
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+__device__ __forceinline__ void reg_fence64(uint32_t (&r)[64]) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // ---------------------------------------------------------------------------- radix key

@@ -14,8 +14,8 @@ struct PrepArgs {
   const int32_t *row_req;
   const int32_t *row_bound;
   int32_t R, Q, pt_stride, max_bound, kv_dtype;
-  uint32_t *hist_target;   // first-digit histogram the scoring kernel will fill (cleared here)
-  int32_t clear_select;    // also clear the selection state (hist2, rowsel)
+  uint32_t *hist_target;   // first-digit histogram the scoring kernel will fill (cleared here), or null
+  int32_t clear_select;    // also clear the selection state (rowsel)
   Workspace ws;
 };
 
@@ -26,7 +26,7 @@ struct ScoreArgs {
   int32_t pt_stride;
   float *scores;
   int64_t ld;
-  uint32_t *hist;          // [R][64] first-digit histogram target (never null)
+  uint32_t *hist;          // [R][64] first-digit histogram target, or null
   Workspace ws;
   uint64_t wait_limit_ns;
   int32_t stall_first_handoff;
@@ -37,7 +37,6 @@ struct SelectArgs {
   int64_t ld;
   const int32_t *bound;    // effective bounds [R]
   int32_t R, K, max_bound;
-  const uint32_t *hist1;   // [R][64]
   int32_t *out_idx;        // [R][K]
   Workspace ws;
 };
@@ -45,10 +44,11 @@ struct SelectArgs {
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
 cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
                          cudaStream_t stream);
-// Selection: clear state (and bounds copy) when not done by the prep launch.
-cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, uint32_t *hist1_to_clear,
-                                cudaStream_t stream);
-cudaError_t launch_first_hist(const SelectArgs &a, uint32_t *hist1, cudaStream_t stream);
-cudaError_t launch_select(const SelectArgs &a, cudaStream_t stream);
+// Selection.  idx_topk: clear the state and copy the bounds, build the 12-bit
+// histogram of the given scores (from the first-digit histogram `coarse` when
+// given).  Both paths end in the collect launch (with the per-row finish).
+cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, cudaStream_t stream);
+cudaError_t launch_hist12(const SelectArgs &a, const uint32_t *coarse, cudaStream_t stream);
+cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream);
 
 }  // namespace idx

@@ -142,7 +142,8 @@ __device__ void plan_block(const PrepArgs &a) {
 // One row's query as the MMA B operand plus its weights.
 //  E4M3 cache: per head, q * 2^e (e a power of two putting the head's largest |q|
 //  in [128, 256)) is split exactly into hi + lo, both E4M3; the MMA runs both
-//  terms against the E4M3 keys, and w * 2^-e undoes the prescale.  A bf16 value
+//  terms against the E4M3 keys, and w * 2^-e undoes the prescale.  The weights
+//  are also halved (exactly): the scoring epilogue forms 2 relu(d) as d + |d|.  A bf16 value
 //  has 8 significant bits and an E4M3 value 4: hi takes the top 4 (round to
 //  nearest) and the remainder, at most 8 units of the bf16 last place, fits the
 //  4 bits of lo, so the split is exact wherever lo is not subnormal.
@@ -197,25 +198,23 @@ __device__ void prep_row(const PrepArgs &a, int r) {
     vl.y = lo[4] | (lo[5] << 8) | (lo[6] << 16) | (static_cast<uint32_t>(lo[7]) << 24);
     *reinterpret_cast<uint2 *>(op0 + off) = vh;
     *reinterpret_cast<uint2 *>(op1 + off) = vl;
-    if ((threadIdx.x & 15) == 0) ws.wq[r * kHeads + h] = ldexpf(a.w[r * kHeads + h], -e);
+    if ((threadIdx.x & 15) == 0) ws.wq[r * kHeads + h] = ldexpf(a.w[r * kHeads + h], -e - 1);
   } else {
     // dims d0..d0+7 = 16 bytes: one chunk of K block d0 / 64.
     const int kb = d0 >> 6;
     const uint32_t off = swz128(h, (d0 & 63) * 2);
     const uint4 raw = *reinterpret_cast<const uint4 *>(q + h * kDim + d0);
     *reinterpret_cast<uint4 *>((kb == 0 ? op0 : op1) + off) = raw;
-    if ((threadIdx.x & 15) == 0) ws.wq[r * kHeads + h] = a.w[r * kHeads + h];
+    if ((threadIdx.x & 15) == 0) ws.wq[r * kHeads + h] = ldexpf(a.w[r * kHeads + h], -1);
   }
 }
 
 __device__ void clear_row_state(const PrepArgs &a, int r) {
   const Workspace &ws = a.ws;
   if (a.hist_target != nullptr && threadIdx.x < 64) a.hist_target[r * 64 + threadIdx.x] = 0u;
-  if (a.clear_select) {
-    for (int i = threadIdx.x; i < 4096; i += blockDim.x) ws.hist2[static_cast<int64_t>(r) * 4096 + i] = 0u;
-    if (threadIdx.x < sizeof(RowSelect) / 4)
-      reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
-  }
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+  if (a.clear_select && threadIdx.x < sizeof(RowSelect) / 4)
+    reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
 }
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {

@@ -1,27 +1,31 @@
 // The scoring scan: paged key loads (TMA), the tensor-core contraction
 // (tcgen05, accumulator in TMEM), the ReLU-weighted head reduction, the score
-// store and the fused first-digit histogram.
+// store and the fused score histogram.
 //
 // sglang PR 48224 page (sgl-amd-mono #86): "scores every cached key of each row"
 // (section Motivation, first paragraph); rows of one request read each key once
 // (section Modifications, commit 1); the store drops "keys at or past a row's
-// bound" (commit 2); each stored score's first radix digit radix_key >> 26 is
-// counted in 64 bins per row during the scan, which the selection then uses
-// instead of a pass of its own (commit 4, the score_hist mailbox).
+// bound" (commit 2); the first radix digit radix_key >> 26 of every stored score
+// is counted in 64 bins per row during the scan, so the selection needs no pass
+// of its own for it (commit 4, the score_hist mailbox).  Here the scan counts the
+// top 12 bits of the radix key; the first digit's 64 bins are its marginal.
 //
 // GB300 layout of the work.  One persistent CTA per SM walks an even share of
 // the launch's tiles; a tile is 128 consecutive key positions (two pages) of one
 // row group (up to 4 rows of one request).  For a tile the contraction is
-//     D[key][row*64 + head] = <k_key, q_row_head>      (M = 128, N = 64 * rows, K = 128)
+//     D[key][row*64 + head] = <k_key, q_row_head>      (M = 128, N = 64 * rows)
 // so a TMEM lane holds one key and each epilogue thread reduces its key's 64
-// head values per row in registers.
-//   warp 0      producer: page ids, TMA of the key pages into an smem ring, and
-//               the group's query operand (bulk copy) on group changes;
-//   warp 1      MMA issuer (one thread) and TMEM owner;
-//   warps 2..9  epilogue, two sets of four; set s handles the tiles whose local
-//               index is s mod 2, in TMEM accumulator buffer s.
+// head values of a row in registers.
+//   warp 0      producer: page ids, TMA of the key pages into an smem ring, the
+//               keys' scales into a second ring, and the group's query operand
+//               (bulk copy) on group changes;
+//   warp 1      MMA issuer (one thread) and TMEM owner; two accumulators in TMEM,
+//               so the MMA of tile k+1 runs while tile k's epilogue reads;
+//   warps 2..17 epilogue, four sets of four (one warp per TMEM lane quarter);
+//               set i reduces row i of the group for every tile, so each warp
+//               keeps one row's weights and one row's histogram.
 // E4M3 cache: keys feed tcgen05.mma kind::f8f6f4 straight from the TMA ring; the
-// query is split exactly into two E4M3 terms (prep.cu), run as K = 256.
+// query is split exactly into two E4M3 terms (prep.cu), run as K = 2 x 128.
 // bf16 cache: keys and query are bf16, kind::f16, K = 128.
 #include "idx_device.cuh"
 #include "launch.h"
@@ -29,42 +33,57 @@
 namespace idx {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kBOperandBytes = 2 * kMaxGroupRows * kRowOperandBytes;  // two K blocks
 constexpr int kTmemCols = 512;                                        // two accumulators of 256
+constexpr int kScaleSlots = 8;
+constexpr int kHistWords = kHistBins / 2;   // two 16-bit counters per word
+constexpr int kFlushTiles = 256;            // 256 tiles x 128 keys < 65536: no counter overflows
 
 template <int KV>
 struct Cfg {
   static constexpr int kStageBytes = KV == IDX_KV_E4M3 ? kTileKeys * kDim : kTileKeys * kDim * 2;
-  static constexpr int kStages = KV == IDX_KV_E4M3 ? 8 : 4;
+  static constexpr int kStages = KV == IDX_KV_E4M3 ? 6 : 3;
   static constexpr int kPageBytes = kStageBytes / 2;
 };
 
 struct Barriers {
   uint64_t full[8];
   uint64_t empty[8];
+  uint64_t sfull[kScaleSlots];
+  uint64_t sempty[kScaleSlots];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t bfull;
   uint64_t bfree;
   uint64_t drain;
+  uint64_t hdone[4];     // per epilogue set: its four warps finished adding to the histogram
+  uint64_t hflushed[4];  // per epilogue set: its four warps finished flushing it
   uint32_t tmem_base;
   int abort;
 };
 
 template <int KV>
-constexpr int smem_bytes() {
-  return 1024 /* alignment slack */ + kBOperandBytes + Cfg<KV>::kStages * Cfg<KV>::kStageBytes +
-         static_cast<int>(sizeof(Barriers)) + kEpiWarps * kMaxGroupRows * 64 * 4;
-}
+struct Smem {
+  static constexpr int kB = 0;
+  static constexpr int kA = kB + kBOperandBytes;
+  static constexpr int kHist = kA + Cfg<KV>::kStages * Cfg<KV>::kStageBytes;
+  static constexpr int kScales = kHist + kMaxGroupRows * kHistWords * 4;
+  static constexpr int kW = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
+  static constexpr int kBars = kW + kEpiWarps * kHeads * 4;
+  static constexpr int kBytes = kBars + static_cast<int>(sizeof(Barriers));
+  static constexpr int kDynamic = kBytes + 1024;  // alignment slack
+};
+static_assert(Smem<IDX_KV_E4M3>::kDynamic <= 227 * 1024, "shared memory");
+static_assert(Smem<IDX_KV_BF16>::kDynamic <= 227 * 1024, "shared memory");
 
 // Walks the groups of a CTA's tile range in order.
 struct GroupCursor {
   const Group *groups;
   int num_groups;
-  int g;          // current group
-  int next_begin; // first tile of the next group
+  int g;
+  int next_begin;
   __device__ void seek(const Group *gs, int ng, int t) {
     groups = gs;
     num_groups = ng;
@@ -76,7 +95,7 @@ struct GroupCursor {
     g = lo;
     next_begin = (g + 1 < ng) ? gs[g + 1].tile_begin : 0x7fffffff;
   }
-  __device__ bool advance(int t) {  // true if the group changed
+  __device__ bool advance(int t) {
     bool changed = false;
     while (t >= next_begin) {
       ++g;
@@ -92,25 +111,68 @@ __device__ __forceinline__ void set_abort(Barriers *bars, uint32_t *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
+// sum_h w[h] * relu(v[h]) over 32 heads, with the weights already halved:
+// v + |v| = 2 relu(v) exactly, one FADD (the |v| is an operand modifier) on the
+// FMA pipe instead of a max on the ALU pipe, then packed FMAs into four
+// accumulators so that the FMAs of one row form four short chains.
+__device__ __forceinline__ void relu_dot32(const uint32_t (&v)[32], const float4 *w, float2 (&acc)[4]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 wv = w[c];
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float d = __uint_as_float(v[4 * c + i]);
+      e[i] = d + fabsf(d);
+    }
+    acc[(2 * c) & 3] = __ffma2_rn(make_float2(e[0], e[1]), make_float2(wv.x, wv.y), acc[(2 * c) & 3]);
+    acc[(2 * c + 1) & 3] = __ffma2_rn(make_float2(e[2], e[3]), make_float2(wv.z, wv.w), acc[(2 * c + 1) & 3]);
+  }
+}
+
+// ReLU(s * d) = s * min(d, 0) for a negative scale s: the other branch
+// (d - |d| = 2 min(d, 0), again with the halved weights).
+__device__ __forceinline__ void relu_dot32_signed(const uint32_t (&v)[32], const float4 *w, bool neg,
+                                                  float2 (&acc)[4]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 wv = w[c];
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float d = __uint_as_float(v[4 * c + i]);
+      e[i] = neg ? d - fabsf(d) : d + fabsf(d);
+    }
+    acc[0] = __ffma2_rn(make_float2(e[0], e[1]), make_float2(wv.x, wv.y), acc[0]);
+    acc[1] = __ffma2_rn(make_float2(e[2], e[3]), make_float2(wv.z, wv.w), acc[1]);
+  }
+}
+
 template <int KV>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const ScoreArgs a) {
   using C = Cfg<KV>;
+  using S = Smem<KV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sB0 = smem;                                   // K block 0 of the group's query operand
-  uint8_t *sB1 = smem + kBOperandBytes / 2;              // K block 1
-  uint8_t *sA = smem + kBOperandBytes;                   // key ring
-  Barriers *bars = reinterpret_cast<Barriers *>(sA + C::kStages * C::kStageBytes);
-  uint32_t *shist = reinterpret_cast<uint32_t *>(bars + 1);  // [warp][row][64]
+  uint8_t *sB0 = smem + S::kB;                          // K block 0 of the group's query operand
+  uint8_t *sB1 = smem + S::kB + kBOperandBytes / 2;     // K block 1
+  uint8_t *sA = smem + S::kA;                           // key ring
+  uint32_t *shist = reinterpret_cast<uint32_t *>(smem + S::kHist);   // [row][2048] packed 16-bit counts
+  float *sscale = reinterpret_cast<float *>(smem + S::kScales);     // [slot][128]
+  float *sw = reinterpret_cast<float *>(smem + S::kW);              // [epilogue warp][64]
+  Barriers *bars = reinterpret_cast<Barriers *>(smem + S::kBars);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Workspace &ws = a.ws;
+
+  grid_dependency_wait();   // the plan and the query operands come from the prep launch
   const int total_tiles = ws.plan->total_tiles;
   const int num_groups = ws.plan->num_groups;
   const int64_t t0 = static_cast<int64_t>(total_tiles) * blockIdx.x / gridDim.x;
   const int64_t t1 = static_cast<int64_t>(total_tiles) * (blockIdx.x + 1) / gridDim.x;
+  grid_dependency_trigger();
   if (t0 >= t1) return;  // uniform for the CTA: nothing allocated yet
 
   if (threadIdx.x == 0) {
@@ -118,9 +180,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
+    for (int s = 0; s < kScaleSlots; ++s) {
+      mbar_init(&bars->sfull[s], 1);
+      mbar_init(&bars->sempty[s], kEpiWarps);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->tfull[s], 1);
-      mbar_init(&bars->tempty[s], 4);
+      mbar_init(&bars->tempty[s], kEpiWarps);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->hdone[s], 4);
+      mbar_init(&bars->hflushed[s], 4);
     }
     mbar_init(&bars->bfull, 1);
     mbar_init(&bars->bfree, 1);
@@ -128,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     bars->abort = 0;
     fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < kEpiWarps * kMaxGroupRows * 64; i += kThreads) shist[i] = 0u;
+  for (int i = threadIdx.x; i < kMaxGroupRows * kHistWords; i += kThreads) shist[i] = 0u;
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -147,12 +217,20 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       const uint64_t policy = l2_evict_first_policy();
       GroupCursor cur;
       cur.seek(ws.groups, num_groups, static_cast<int>(t0));
-      int cur_g = -1, req = 0, L = 0, nswitch = 0;
+      int cur_g = -1, req = 0, L = 0, nswitch = 0, tile_begin = 0;
+      // page ids of a tile: the pages of positions j*128 and j*128 + 64, or -1 past L
+      auto tile_pages = [&](int j, int32_t (&p)[2]) {
+        for (int h = 0; h < 2; ++h) {
+          const int64_t first = static_cast<int64_t>(j) * kTileKeys + h * kPage;
+          p[h] = first < L ? a.page_table[static_cast<int64_t>(req) * a.pt_stride + first / kPage] : -2;
+        }
+      };
+      int32_t next_pages[2] = {-2, -2};
       int k = 0;
       for (int64_t t = t0; t < t1; ++t, ++k) {
-        cur.advance(static_cast<int>(t));
-        const Group grp = ws.groups[cur.g];
-        if (cur.g != cur_g) {
+        bool fresh = false;
+        if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
+          const Group grp = ws.groups[cur.g];
           if (cur_g >= 0 && !mbar_wait(&bars->bfree, (nswitch - 1) & 1, limit, abort)) {
             set_abort(bars, ws.status);
             break;
@@ -164,35 +242,47 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           cur_g = cur.g;
           req = grp.req;
           L = grp.L;
+          tile_begin = grp.tile_begin;
           ++nswitch;
+          fresh = true;
         }
+        const int j = static_cast<int>(t) - tile_begin;
+        int32_t pages[2];
+        if (fresh) {
+          tile_pages(j, pages);
+        } else {
+          pages[0] = next_pages[0];
+          pages[1] = next_pages[1];
+        }
+        // the next tile's page ids load while this tile waits for its slot
+        if (t + 1 < t1 && static_cast<int>(t) + 1 < cur.next_begin) tile_pages(j + 1, next_pages);
         const int s = k % C::kStages;
-        if (!mbar_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1, limit, abort)) {
+        const int ss = k % kScaleSlots;
+        if (!mbar_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1, limit, abort) ||
+            (KV == IDX_KV_E4M3 && !mbar_wait(&bars->sempty[ss], ((k / kScaleSlots) & 1) ^ 1, limit, abort))) {
           set_abort(bars, ws.status);
           break;
         }
-        const int j = static_cast<int>(t) - grp.tile_begin;
-        int32_t pages[2];
         uint32_t bytes = 0;
         for (int h = 0; h < 2; ++h) {
-          pages[h] = -1;
-          const int64_t first = static_cast<int64_t>(j) * kTileKeys + h * kPage;
-          if (first < L) {
-            const int32_t p = a.page_table[static_cast<int64_t>(req) * a.pt_stride + first / kPage];
-            if (p >= 0 && p < a.P) {
-              pages[h] = p;
-              bytes += C::kPageBytes;
-            } else {
-              flag_status(ws.status, kStatusBadPage);
-            }
+          if (pages[h] == -2) {
+            pages[h] = -1;
+          } else if (pages[h] >= 0 && pages[h] < a.P) {
+            bytes += C::kPageBytes;
+          } else {
+            pages[h] = -1;
+            flag_status(ws.status, kStatusBadPage);
           }
         }
         mbar_arrive_expect_tx(&bars->full[s], bytes);
+        if (KV == IDX_KV_E4M3) mbar_arrive_expect_tx(&bars->sfull[ss], (bytes / C::kPageBytes) * (kPage * 4));
         uint8_t *dst = sA + s * C::kStageBytes;
         for (int h = 0; h < 2; ++h) {
           if (pages[h] < 0) continue;
           if (KV == IDX_KV_E4M3) {
             tma_load_2d(dst + h * (kPage * kDim), &kmap, 0, pages[h] * kPage, &bars->full[s], policy);
+            bulk_load(sscale + ss * kTileKeys + h * kPage, a.k_scale + static_cast<int64_t>(pages[h]) * kPage,
+                      kPage * 4, &bars->sfull[ss]);
           } else {
             tma_load_2d(dst + h * (kPage * 128), &kmap, 0, pages[h] * kPage, &bars->full[s], policy);
             tma_load_2d(dst + kTileKeys * 128 + h * (kPage * 128), &kmap, 64, pages[h] * kPage, &bars->full[s],
@@ -207,6 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         const int last_use = issued - 1 - ((issued - 1 - s) % C::kStages);
         if (!mbar_wait(&bars->full[s], (last_use / C::kStages) & 1, limit, &never))
           flag_status(ws.status, kStatusTimeout);
+      }
+      if (KV == IDX_KV_E4M3) {
+        for (int s = 0; s < kScaleSlots && s < issued; ++s) {
+          const int last_use = issued - 1 - ((issued - 1 - s) % kScaleSlots);
+          if (!mbar_wait(&bars->sfull[s], (last_use / kScaleSlots) & 1, limit, &never))
+            flag_status(ws.status, kStatusTimeout);
+        }
       }
       if (nswitch > 0 && !mbar_wait(&bars->bfull, (nswitch - 1) & 1, limit, &never))
         flag_status(ws.status, kStatusTimeout);
@@ -265,110 +362,131 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   } else {
     // ------------------------------------------------------------------ epilogue
     const int ew = warp - 2;
-    const int set = ew >> 2;
-    const int quarter = warp & 3;              // TMEM lane quarter this warp may read
-    uint32_t *hist = shist + ew * kMaxGroupRows * 64;
+    const int set = ew >> 2;                 // the group row this warp reduces
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may read
+    const int wq4 = ew & 3;                  // this warp's share of the row's histogram flush
+    float *myw = sw + ew * kHeads;
+    uint32_t *h = shist + set * kHistWords;
     GroupCursor cur;
     cur.seek(ws.groups, num_groups, static_cast<int>(t0));
     int cur_g = -1;
     Group grp;
     grp.nrows = 0;
-    int k = 0;
-    auto flush = [&]() {
+    grp.row0 = 0;
+    bool mine = false;
+    int32_t bnd = 0;
+    int flushes = 0;
+    int tiles_since_flush = 0;
+    bool ok = true;
+
+    // The set's histogram row goes to global memory (12-bit counts and, when asked,
+    // the 64-bin first digit) and is cleared; the set's four warps meet before and after.
+    auto flush = [&]() -> bool {
       __syncwarp();
-      for (int i = 0; i < grp.nrows; ++i) {
-        for (int d = lane; d < 64; d += 32) {
-          const uint32_t c = hist[i * 64 + d];
-          if (c) {
-            atomicAdd(&a.hist[static_cast<int64_t>(grp.row0 + i) * 64 + d], c);
-            hist[i * 64 + d] = 0u;
+      if (lane == 0) mbar_arrive(&bars->hdone[set]);
+      if (!mbar_wait(&bars->hdone[set], flushes & 1, limit, abort)) return false;
+      if (mine) {
+        const int64_t grow = grp.row0 + set;
+        for (int d = wq4 * 16; d < wq4 * 16 + 16; ++d) {   // 16 first digits per warp
+          const uint32_t wv = h[d * 32 + lane];
+          const uint32_t lo = wv & 0xFFFFu, hi = wv >> 16;
+          if (wv) {
+            h[d * 32 + lane] = 0u;
+            if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
+            if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
+          }
+          if (a.hist != nullptr) {
+            const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
+            if (lane == 0 && dsum) atomicAdd(&a.hist[grow * 64 + d], dsum);
           }
         }
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->hflushed[set]);
+      const bool r = mbar_wait(&bars->hflushed[set], flushes & 1, limit, abort);
+      ++flushes;
+      tiles_since_flush = 0;
+      return r;
     };
-    for (int64_t t = t0; t < t1; ++t, ++k) {
-      cur.advance(static_cast<int>(t));
-      if (cur.g != cur_g) {
-        if (cur_g >= 0) flush();
+
+    for (int64_t t = t0; t < t1; ++t) {
+      const int k = static_cast<int>(t - t0);
+      if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
+        if (cur_g >= 0 && !flush()) {
+          ok = false;
+          break;
+        }
         cur_g = cur.g;
         grp = ws.groups[cur_g];
+        mine = set < grp.nrows;
+        bnd = mine ? ws.bound_eff[grp.row0 + set] : 0;
+        __syncwarp();
+        if (mine) {
+          const float2 v = reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(grp.row0 + set) * kHeads)[lane];
+          reinterpret_cast<float2 *>(myw)[lane] = v;
+        }
+        __syncwarp();
+      } else if (tiles_since_flush >= kFlushTiles) {
+        if (!flush()) {
+          ok = false;
+          break;
+        }
       }
-      if ((k & 1) != set) continue;
+      ++tiles_since_flush;
       const int j = static_cast<int>(t) - grp.tile_begin;
       const int64_t pos = static_cast<int64_t>(j) * kTileKeys + quarter * 32 + lane;
-      const bool valid = pos < grp.L;
+      const int acc = k & 1;
+      const int ss = k % kScaleSlots;
       float scale = 1.0f;
-      if (KV == IDX_KV_E4M3 && valid) {
-        const int32_t p = a.page_table[static_cast<int64_t>(grp.req) * a.pt_stride + pos / kPage];
-        scale = (p >= 0 && p < a.P) ? __ldg(&a.k_scale[static_cast<int64_t>(p) * kPage + (pos % kPage)]) : 0.0f;
+      if (KV == IDX_KV_E4M3) {
+        if (!mbar_wait(&bars->sfull[ss], (k / kScaleSlots) & 1, limit, abort)) {
+          set_abort(bars, ws.status);
+          ok = false;
+          break;
+        }
+        scale = sscale[ss * kTileKeys + quarter * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sempty[ss]);
       }
-      if (!mbar_wait(&bars->tfull[set], (k >> 1) & 1, limit, abort)) {
+      if (!mbar_wait(&bars->tfull[acc], (k >> 1) & 1, limit, abort)) {
         set_abort(bars, ws.status);
+        ok = false;
         break;
       }
       tc_fence_after();
-      const bool neg_scale = valid && scale < 0.0f;
-      const bool any_neg = __any_sync(0xffffffffu, neg_scale);
-      for (int i = 0; i < grp.nrows; ++i) {
-        const int row = grp.row0 + i;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + set * 256 + i * 64;
-        uint32_t v0[32], v1[32];
-        tmem_ld32(taddr, v0);
-        tmem_ld32(taddr + 32, v1);
-        tmem_wait_ld();
-        reg_fence(v0);
-        reg_fence(v1);
-        const float4 *wrow = reinterpret_cast<const float4 *>(ws.wq + static_cast<int64_t>(row) * kHeads);
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        if (!any_neg) {
+      float score = 0.f;
+      const bool valid = pos < grp.L;
+      if (mine) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256 + set * 64;
+        const bool neg = valid && scale < 0.0f;
+        const bool any_neg = __any_sync(0xffffffffu, neg);
+        const float4 *w4 = reinterpret_cast<const float4 *>(myw);
+        float2 accs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 wv = __ldg(wrow + c);
-            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(v0[4 * c + 0]), 0.f), acc0);
-            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(v0[4 * c + 1]), 0.f), acc1);
-            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(v0[4 * c + 2]), 0.f), acc2);
-            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(v0[4 * c + 3]), 0.f), acc3);
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 wv = __ldg(wrow + 8 + c);
-            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(v1[4 * c + 0]), 0.f), acc0);
-            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(v1[4 * c + 1]), 0.f), acc1);
-            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(v1[4 * c + 2]), 0.f), acc2);
-            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(v1[4 * c + 3]), 0.f), acc3);
-          }
-        } else {
-          // ReLU(s * d) = s * min(d, 0) when s < 0.
-          const bool nz = neg_scale;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float4 wv = __ldg(wrow + c);
-            const uint32_t *v = c < 8 ? v0 : v1;
-            const int o = (c & 7) * 4;
-            const float e0 = __uint_as_float(v[o + 0]), e1 = __uint_as_float(v[o + 1]);
-            const float e2 = __uint_as_float(v[o + 2]), e3 = __uint_as_float(v[o + 3]);
-            acc0 = fmaf(wv.x, nz ? fminf(e0, 0.f) : fmaxf(e0, 0.f), acc0);
-            acc1 = fmaf(wv.y, nz ? fminf(e1, 0.f) : fmaxf(e1, 0.f), acc1);
-            acc2 = fmaf(wv.z, nz ? fminf(e2, 0.f) : fmaxf(e2, 0.f), acc2);
-            acc3 = fmaf(wv.w, nz ? fminf(e3, 0.f) : fmaxf(e3, 0.f), acc3);
-          }
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld32(taddr + half * 32, v);
+          tmem_wait_ld();
+          reg_fence(v);
+          if (!any_neg) relu_dot32(v, w4 + half * 8, accs);
+          else relu_dot32_signed(v, w4 + half * 8, neg, accs);
         }
-        if (i == grp.nrows - 1) {
-          // Accumulator buffer fully read: hand it back to the MMA issuer.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[set]);
-        }
-        const float score = ((acc0 + acc1) + (acc2 + acc3)) * scale;
-        const bool keep = valid && pos < ws.bound_eff[row];
-        if (keep) a.scores[static_cast<int64_t>(row) * a.ld + pos] = score;
-        const uint32_t digit = keep ? (radix_key(score) >> 26) : 64u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (digit < 64u && lane == __ffs(peers) - 1) atomicAdd(&hist[i * 64 + digit], __popc(peers));
+        score = (((accs[0].x + accs[0].y) + (accs[1].x + accs[1].y)) + ((accs[2].x + accs[2].y) + (accs[3].x + accs[3].y))) * scale;
+      }
+      // Accumulator read: hand it back to the MMA issuer.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (mine) {
+        const bool keep = valid && pos < bnd;
+        if (keep) a.scores[static_cast<int64_t>(grp.row0 + set) * a.ld + pos] = score;
+        const uint32_t bin = keep ? (radix_key(score) >> (32 - kHistBits)) : 0xFFFFFFFFu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (keep && lane == __ffs(peers) - 1)
+          atomicAdd(&h[bin >> 1], static_cast<uint32_t>(__popc(peers)) << ((bin & 1) * 16));
       }
     }
-    if (cur_g >= 0) flush();
+    if (ok && cur_g >= 0) flush();
   }
 
   // Every role is done (or gave up); release TMEM.
@@ -383,14 +501,23 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 template <int KV>
 cudaError_t launch_kv(const CUtensorMap &kmap, const ScoreArgs &a, int num_ctas, cudaStream_t stream) {
   static bool configured = false;
-  constexpr int bytes = smem_bytes<KV>();
+  constexpr int bytes = Smem<KV>::kDynamic;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(score_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  score_kernel<KV><<<num_ctas, kThreads, bytes, stream>>>(kmap, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_kernel<KV>, kmap, a);
 }
 
 }  // namespace

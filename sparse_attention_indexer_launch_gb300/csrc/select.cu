@@ -1,60 +1,64 @@
 // Exact top-K selection by radix digits.
 //
 // sglang PR 48224 page (sgl-amd-mono #86): each row's "exact top-2048" (section
-// Motivation, first paragraph) is chosen by radix selection over slices of at
-// most 8,192 keys whose first digit is radix_key >> 26 in 64 bins (section
-// Motivation, fourth bullet; section Modifications, commit 4, where that
-// histogram comes from the scoring stage instead of a pass of its own).  The
-// later digits, the counts and the placement are the selection's own.
+// Motivation, first paragraph) is chosen by radix selection over slices of the
+// row's keys, with the first digit radix_key >> 26 counted in 64 bins during the
+// scoring (section Motivation, fourth bullet; section Modifications, commit 4);
+// the later digits, the counts and the placement follow in the selection.
 //
-// Order of keys: by the 64-bit composite (radix_key(score) << 32) | ~position,
+// Order of keys: the 64-bit composite (radix_key(score) << 32) | ~position,
 // larger first, i.e. score descending and, among equal scores, position
-// ascending; the top K composites are exactly the wanted set, so ties at the
+// ascending.  The top K composites are exactly the wanted set, so ties at the
 // k-th value go to the lowest positions.
 //
-// Kernels, each over (slice, row) unless noted:
-//   first_hist   only when no histogram is given: 64-bin first-digit histogram;
-//   hist2        the 64-bin histogram fixes the first digit d1 holding the k-th
-//                key; this pass counts the next 12 bits of the keys in bin d1;
-//                the slice that arrives last for its row finds the 18-bit prefix
-//                holding the k-th key (no waiting: an arrival counter);
-//   collect      appends every key above that prefix (winners, < K of them) and
-//                every key on it (threshold candidates);
-//   finish (row) sorts winners and candidates and writes the first min(K, bound)
-//                positions, -1 after.  When a row has more candidates than the
-//                candidate buffer holds (many equal scores), it resolves the
-//                remaining 46 composite bits digit by digit over the row itself.
+// Data flow (one row; many rows run side by side):
+//   hist12   the histogram of the top 12 bits of radix_key (the scoring kernel
+//            fuses it; idx_topk on given scores builds it with hist12_kernel,
+//            needing only the 64-bin first digit when that is given).
+//   collect  (slices of kSlice keys, one CTA each) finds the 12-bit bin T that
+//            holds the k-th key, appends every key above T (the winners, fewer
+//            than K) and every key in T (the candidates).  The CTA that finishes
+//            last for its row (an arrival counter: nothing waits) then
+//   finish   picks the K - winners best candidates by a radix select over the
+//            remaining 52 composite bits in shared memory, sorts the K keys and
+//            writes the positions, -1 past min(K, bound).  A row with more
+//            candidates than the buffer holds (thousands of equal scores) is
+//            resolved digit by digit over the row's scores instead.
 #include "idx_device.cuh"
 #include "launch.h"
 
 namespace idx {
 namespace {
 
-constexpr int kSlice = 8192;
-constexpr int kSelThreads = 256;
-constexpr int kFinishThreads = 512;
-constexpr int kFinishCap = 8192;   // >= IDX_MAX_K + kTieCap, power of two
+constexpr int kSlice = 16384;
+constexpr int kThreads = 1024;
+constexpr int kHistThreads = 512;
+constexpr int kSortCap = 2048;            // = IDX_MAX_K, power of two
+// dynamic shared memory of the collect/finish kernel
+constexpr int kFinishSmem = (kTieCap + kSortCap) * 8;
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t pos) {
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
 }
 
-__device__ __forceinline__ int nslices(int32_t bound) { return (bound + kSlice - 1) / kSlice; }
+__device__ __forceinline__ int nslices(int32_t bound) { return bound > 0 ? (bound + kSlice - 1) / kSlice : 1; }
 
-// Among nbins bins in descending bin order, the bin holding the need-th key:
-// above < need <= above + hist[bin], above = keys in higher bins.  Block-wide;
-// every thread returns the result.  nbins = 64 uses one warp's worth of work,
-// but all threads must call it.
+// Among nbins bins taken in descending bin order, the bin holding the need-th key:
+// above < need <= above + hist[bin], above = keys in higher bins.  Block-wide:
+// every thread must call it and every thread gets the result.
 __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_t *out_bin, uint32_t *out_above,
-                         uint32_t *scratch /* >= 34 words */) {
+                         uint32_t *scratch /* >= 34 words of shared memory */) {
   const int per = (nbins + blockDim.x - 1) / blockDim.x;
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    scratch[32] = 0u;
+    scratch[33] = 0u;
+  }
   uint32_t sum = 0;
   for (int m = 0; m < per; ++m) {
     const int i = tid * per + m;
     if (i < nbins) sum += hist[nbins - 1 - i];
   }
-  // exclusive scan of sum over the block
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t incl = sum;
 #pragma unroll
@@ -96,13 +100,12 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
   __syncthreads();
 }
 
-// ---------------------------------------------------------------------------- state
-__global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound, uint32_t *hist1) {
+// ---------------------------------------------------------------------------- idx_topk front
+__global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound) {
   const int r = blockIdx.x;
   const Workspace &ws = a.ws;
-  for (int i = threadIdx.x; i < 4096; i += blockDim.x) ws.hist2[static_cast<int64_t>(r) * 4096 + i] = 0u;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
   if (threadIdx.x < sizeof(RowSelect) / 4) reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
-  if (hist1 != nullptr && threadIdx.x < 64) hist1[r * 64 + threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     const int32_t b = row_bound[r];
     const int32_t be = max(0, min(b, a.max_bound));
@@ -111,77 +114,38 @@ __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) first_hist_kernel(const SelectArgs a, uint32_t *hist1) {
-  __shared__ uint32_t h[64];
-  const int r = blockIdx.y;
-  const int32_t B = a.bound[r];
-  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
-  if (threadIdx.x < 64) h[threadIdx.x] = 0u;
-  __syncthreads();
-  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
-  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  for (int64_t base = begin; base < end; base += kSelThreads) {
-    const int64_t pos = base + threadIdx.x;
-    const uint32_t d = pos < end ? (radix_key(row[pos]) >> 26) : 64u;
-    const uint32_t peers = __match_any_sync(0xffffffffu, d);
-    if (d < 64u && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[d], __popc(peers));
-  }
-  __syncthreads();
-  if (threadIdx.x < 64 && h[threadIdx.x]) atomicAdd(&hist1[r * 64 + threadIdx.x], h[threadIdx.x]);
-}
-
-// ---------------------------------------------------------------------------- second digit
-__global__ void __launch_bounds__(kSelThreads) hist2_kernel(const SelectArgs a) {
-  __shared__ uint32_t h[4096];
+// The 12-bit histogram of given scores.  With a first-digit histogram `coarse`,
+// only the keys of the first digit that holds the k-th key are counted finely;
+// every other digit's count goes to that digit's lowest 12-bit bin, which keeps
+// every count "above" a bin exact for the threshold search.
+__global__ void __launch_bounds__(kHistThreads) hist12_kernel(const SelectArgs a, const uint32_t *coarse) {
+  __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t scratch[34];
-  __shared__ uint32_t d1_s, above1_s;
-  __shared__ int is_last;
   const int r = blockIdx.y;
   const int32_t B = a.bound[r];
-  if (B <= a.K) return;  // the row keeps all its keys
-  const int ns = nslices(B);
-  if (static_cast<int>(blockIdx.x) >= ns) return;
+  if (B <= a.K || static_cast<int>(blockIdx.x) >= nslices(B)) return;   // rows that keep all keys skip it
   const Workspace &ws = a.ws;
-  for (int i = threadIdx.x; i < 4096; i += kSelThreads) h[i] = 0u;
-  if (threadIdx.x < 64) scratch[threadIdx.x & 31] = 0u;
-  __syncthreads();
-  {
-    uint32_t d1, above1;
-    find_bin(a.hist1 + r * 64, 64, static_cast<uint32_t>(a.K), &d1, &above1, scratch);
-    if (threadIdx.x == 0) {
-      d1_s = d1;
-      above1_s = above1;
-    }
+  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads) h[i] = 0u;
+  uint32_t d1 = 0xFFFFFFFFu;
+  if (coarse != nullptr) {
+    __syncthreads();
+    uint32_t bin, above;
+    find_bin(coarse + r * 64, 64, static_cast<uint32_t>(a.K), &bin, &above, scratch);
+    d1 = bin;
+    if (blockIdx.x == 0 && threadIdx.x < 64 && threadIdx.x != d1 && coarse[r * 64 + threadIdx.x])
+      atomicAdd(&ws.hist12[static_cast<int64_t>(r) * kHistBins + threadIdx.x * 64], coarse[r * 64 + threadIdx.x]);
   }
   __syncthreads();
-  const uint32_t d1 = d1_s;
   const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
   const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
   const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-#pragma unroll 4
-  for (int64_t pos = begin + threadIdx.x; pos < end; pos += kSelThreads) {
+  for (int64_t pos = begin + threadIdx.x; pos < end; pos += kHistThreads) {
     const uint32_t key = radix_key(row[pos]);
-    if ((key >> 26) == d1) atomicAdd(&h[(key >> 14) & 4095u], 1u);
+    if (d1 == 0xFFFFFFFFu || (key >> 26) == d1) atomicAdd(&h[key >> 20], 1u);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 4096; i += kSelThreads)
-    if (h[i]) atomicAdd(&ws.hist2[static_cast<int64_t>(r) * 4096 + i], h[i]);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(&ws.rowsel[r].nslices_done, 1u) == static_cast<uint32_t>(ns - 1));
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < 4096; i += kSelThreads) h[i] = __ldcg(&ws.hist2[static_cast<int64_t>(r) * 4096 + i]);
-  __syncthreads();
-  uint32_t d2, above2;
-  find_bin(h, 4096, static_cast<uint32_t>(a.K) - above1_s, &d2, &above2, scratch);
-  if (threadIdx.x == 0) {
-    ws.rowsel[r].prefix = (d1 << 12) | d2;
-    ws.rowsel[r].above = above1_s + above2;
-    ws.rowsel[r].mode = 1u;
-  }
+  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads)
+    if (h[i]) atomicAdd(&ws.hist12[static_cast<int64_t>(r) * kHistBins + i], h[i]);
 }
 
 // ---------------------------------------------------------------------------- collect
@@ -198,37 +162,15 @@ __device__ __forceinline__ void warp_append(bool take, unsigned long long value,
   if (take && idx < cap) dst[idx] = value;
 }
 
-__global__ void __launch_bounds__(kSelThreads) collect_kernel(const SelectArgs a) {
-  const int r = blockIdx.y;
-  const int32_t B = a.bound[r];
-  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
-  const Workspace &ws = a.ws;
-  const bool take_all = B <= a.K;
-  const uint32_t prefix = take_all ? 0u : ws.rowsel[r].prefix;
-  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
-  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
-  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-  for (int64_t base = begin; base < end; base += kSelThreads) {
-    const int64_t pos = base + threadIdx.x;
-    const bool in = pos < end;
-    const uint32_t key = in ? radix_key(row[pos]) : 0u;
-    const uint32_t p18 = key >> 14;
-    const bool w = in && (take_all || p18 > prefix);
-    const bool t = in && !take_all && p18 == prefix;
-    const unsigned long long c = composite(key, pos);
-    warp_append(w, c, win, &ws.rowsel[r].win_count, static_cast<uint32_t>(a.K));
-    warp_append(t, c, tie, &ws.rowsel[r].tie_count, static_cast<uint32_t>(kTieCap));
-  }
-}
-
-// ---------------------------------------------------------------------------- finish
-__device__ void bitonic_sort_desc(unsigned long long *s, int n /* power of two */) {
+// Bitonic sort, descending, of n (a power of two) keys in shared memory.
+// Stages whose pairs stay inside one warp's 64-key block need only __syncwarp.
+__device__ void bitonic_sort_desc(unsigned long long *s, int n) {
+  const int half = n >> 1;
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
-        const int lo = 2 * stride * (i / stride) + (i % stride);
+      const int lg = __ffs(stride) - 1;
+      for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        const int lo = ((i >> lg) << (lg + 1)) | (i & (stride - 1));
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
         const unsigned long long x = s[lo], y = s[hi];
@@ -237,116 +179,195 @@ __device__ void bitonic_sort_desc(unsigned long long *s, int n /* power of two *
           s[hi] = x;
         }
       }
-      __syncthreads();
+      const int next = stride > 1 ? (stride >> 1) : (size << 1) >> 1;
+      if (stride >= 64 || next >= 64 || half > static_cast<int>(blockDim.x)) __syncthreads();
+      else __syncwarp();
     }
   }
+  __syncthreads();
 }
 
-// Remaining composite bits below the 18-bit prefix: 14 score bits, 32 position bits.
-__device__ __forceinline__ unsigned long long low46(uint32_t key, int64_t pos) {
-  return (static_cast<unsigned long long>(key & 0x3FFFu) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
+// Digits of the low 52 composite bits, most significant first: six of 8 bits, one of 4.
+__device__ __forceinline__ int digit_shift(int d) { return d < 6 ? 44 - 8 * d : 0; }
+__device__ __forceinline__ int digit_width(int d) { return d < 6 ? 8 : 4; }
+
+// Low 52 bits of a candidate's composite (the 12 high bits are the shared bin).
+__device__ __forceinline__ unsigned long long low52(unsigned long long c) { return c & ((1ull << 52) - 1); }
+
+// Picks the `need` largest of n candidates (composites sharing their top 12 bits)
+// by 8-bit digits of the low 52 bits; returns the smallest low-52 value taken.
+__device__ unsigned long long select_candidates(const unsigned long long *cand, int n, uint32_t need,
+                                                uint32_t *h /* 256 */, uint32_t *scratch) {
+  unsigned long long pre = 0ull;
+  for (int d = 0; d < 7; ++d) {
+    const int sh = digit_shift(d), wd = digit_width(d);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long v = low52(cand[i]);
+      if (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd))) continue;
+      atomicAdd(&h[(v >> sh) & ((1u << wd) - 1u)], 1u);
+    }
+    __syncthreads();
+    uint32_t bin, above;
+    find_bin(h, 1 << wd, need, &bin, &above, scratch);
+    need -= above;
+    pre |= static_cast<unsigned long long>(bin) << sh;
+  }
+  return pre;
 }
 
-__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const SelectArgs a) {
-  extern __shared__ unsigned long long sk[];   // kFinishCap entries
-  __shared__ uint32_t h[256];
-  __shared__ uint32_t scratch[34];
-  __shared__ uint32_t count_s;
-  const int r = blockIdx.x;
+__device__ void finish_row(const SelectArgs &a, int r, unsigned long long *sm, uint32_t *h, uint32_t *scratch,
+                           uint32_t T12) {
   const Workspace &ws = a.ws;
   const int32_t B = a.bound[r];
   const int K = a.K;
   const int nout = min(K, B);
-  int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
-  const uint32_t nw = min(ws.rowsel[r].win_count, static_cast<uint32_t>(K));
-  const uint32_t nt_all = B > K ? ws.rowsel[r].tie_count : 0u;
+  unsigned long long *cand = sm;                 // kTieCap
+  unsigned long long *fin = sm + kTieCap;        // kSortCap
+  __shared__ uint32_t count_s;
+  const uint32_t nw = min(__ldcg(&ws.rowsel[r].win_count), static_cast<uint32_t>(kSortCap));
+  const uint32_t nt = B > K ? __ldcg(&ws.rowsel[r].tie_count) : 0u;
   const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
   const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-  uint32_t n = nw;
-  for (uint32_t i = threadIdx.x; i < nw; i += kFinishThreads) sk[i] = win[i];
-  if (nt_all <= static_cast<uint32_t>(kTieCap)) {
-    for (uint32_t i = threadIdx.x; i < nt_all; i += kFinishThreads) sk[nw + i] = tie[i];
-    n = nw + nt_all;
-  } else {
-    // Many keys on the 18-bit prefix: find the exact composite threshold among them.
-    const uint32_t prefix = ws.rowsel[r].prefix;
-    uint32_t need = static_cast<uint32_t>(nout) - nw;
-    unsigned long long pre = 0ull;
-    const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-    const int shifts[6] = {38, 30, 22, 14, 6, 0};
-    const int widths[6] = {8, 8, 8, 8, 8, 6};
-    for (int d = 0; d < 6; ++d) {
-      const int sh = shifts[d], wd = widths[d];
-      for (int i = threadIdx.x; i < 256; i += kFinishThreads) h[i] = 0u;
+  for (uint32_t i = threadIdx.x; i < nw; i += blockDim.x) fin[i] = __ldcg(&win[i]);
+  if (threadIdx.x == 0) count_s = nw;
+  __syncthreads();
+  if (B > K) {
+    const uint32_t need = static_cast<uint32_t>(K) - nw;
+    if (nt <= static_cast<uint32_t>(kTieCap)) {
+      for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) cand[i] = __ldcg(&tie[i]);
       __syncthreads();
-      for (int64_t pos = threadIdx.x; pos < B; pos += kFinishThreads) {
+      const unsigned long long th = select_candidates(cand, static_cast<int>(nt), need, h, scratch);
+      for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) {
+        if (low52(cand[i]) >= th) {
+          const uint32_t at = atomicAdd(&count_s, 1u);
+          if (at < static_cast<uint32_t>(kSortCap)) fin[at] = cand[i];
+        }
+      }
+    } else {
+      // Too many keys in the threshold bin: the same digits, over the row's scores.
+      const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
+      unsigned long long pre = 0ull;
+      uint32_t nd = need;
+      for (int d = 0; d < 7; ++d) {
+        const int sh = digit_shift(d), wd = digit_width(d);
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+        __syncthreads();
+        for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
+          const uint32_t key = radix_key(row[pos]);
+          if ((key >> 20) != T12) continue;
+          const unsigned long long v = low52(composite(key, pos));
+          if (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd))) continue;
+          atomicAdd(&h[(v >> sh) & ((1u << wd) - 1u)], 1u);
+        }
+        __syncthreads();
+        uint32_t bin, above;
+        find_bin(h, 1 << wd, nd, &bin, &above, scratch);
+        nd -= above;
+        pre |= static_cast<unsigned long long>(bin) << sh;
+      }
+      for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
         const uint32_t key = radix_key(row[pos]);
-        if ((key >> 14) != prefix) continue;
-        const unsigned long long v = low46(key, pos);
-        if (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd))) continue;
-        atomicAdd(&h[(v >> sh) & ((1u << wd) - 1u)], 1u);
-      }
-      __syncthreads();
-      uint32_t bin, above;
-      find_bin(h, 1 << wd, need, &bin, &above, scratch);
-      need -= above;
-      pre |= static_cast<unsigned long long>(bin) << sh;
-    }
-    // pre is now the composite (low 46 bits) of the last key taken from the prefix bin.
-    if (threadIdx.x == 0) count_s = nw;
-    __syncthreads();
-    for (int64_t pos = threadIdx.x; pos < B; pos += kFinishThreads) {
-      const uint32_t key = radix_key(row[pos]);
-      if ((key >> 14) != prefix) continue;
-      if (low46(key, pos) >= pre) {
-        const uint32_t idx = atomicAdd(&count_s, 1u);
-        if (idx < static_cast<uint32_t>(kFinishCap)) sk[idx] = composite(key, pos);
+        if ((key >> 20) != T12) continue;
+        const unsigned long long c = composite(key, pos);
+        if (low52(c) >= pre) {
+          const uint32_t at = atomicAdd(&count_s, 1u);
+          if (at < static_cast<uint32_t>(kSortCap)) fin[at] = c;
+        }
       }
     }
-    __syncthreads();
-    n = min(count_s, static_cast<uint32_t>(kFinishCap));
   }
   __syncthreads();
+  const int n = min(static_cast<int>(count_s), kSortCap);
   int p2 = 1;
-  while (p2 < static_cast<int>(n)) p2 <<= 1;
-  for (int i = static_cast<int>(n) + threadIdx.x; i < p2; i += kFinishThreads) sk[i] = 0ull;
+  while (p2 < n) p2 <<= 1;
+  for (int i = n + threadIdx.x; i < p2; i += blockDim.x) fin[i] = 0ull;
   __syncthreads();
-  bitonic_sort_desc(sk, p2);
-  for (int j = threadIdx.x; j < K; j += kFinishThreads)
-    out[j] = (j < nout && j < static_cast<int>(n)) ? static_cast<int32_t>(~static_cast<uint32_t>(sk[j] & 0xFFFFFFFFull)) : -1;
+  bitonic_sort_desc(fin, p2);
+  int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
+  for (int j = threadIdx.x; j < K; j += blockDim.x)
+    out[j] = (j < nout && j < n) ? static_cast<int32_t>(~static_cast<uint32_t>(fin[j] & 0xFFFFFFFFull)) : -1;
+}
+
+__global__ void __launch_bounds__(kThreads) collect_kernel(const SelectArgs a) {
+  extern __shared__ unsigned long long sm[];
+  __shared__ uint32_t h[256];
+  __shared__ uint32_t hist_s[kHistBins];
+  __shared__ uint32_t scratch[34];
+  __shared__ int is_last;
+  grid_dependency_wait();   // scores and the histogram come from the previous launch
+  const int r = blockIdx.y;
+  const int32_t B = a.bound[r];
+  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
+  const Workspace &ws = a.ws;
+  const bool take_all = B <= a.K;
+  uint32_t T12 = 0;
+  if (!take_all) {
+    for (int i = threadIdx.x; i < kHistBins; i += kThreads)
+      hist_s[i] = __ldcg(&ws.hist12[static_cast<int64_t>(r) * kHistBins + i]);
+    __syncthreads();
+    uint32_t above;
+    find_bin(hist_s, kHistBins, static_cast<uint32_t>(a.K), &T12, &above, scratch);
+  }
+  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
+  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
+  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
+  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
+  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
+  for (int64_t base = begin; base < end; base += kThreads) {
+    const int64_t pos = base + threadIdx.x;
+    const bool in = pos < end;
+    const uint32_t key = in ? radix_key(row[pos]) : 0u;
+    const uint32_t bin = key >> 20;
+    const bool w = in && (take_all || bin > T12);
+    const bool t = in && !take_all && bin == T12;
+    const unsigned long long c = composite(key, pos);
+    warp_append(w, c, win, &ws.rowsel[r].win_count, static_cast<uint32_t>(a.K));
+    warp_append(t, c, tie, &ws.rowsel[r].tie_count, static_cast<uint32_t>(kTieCap));
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    is_last = atomicAdd(&ws.rowsel[r].nslices_done, 1u) == static_cast<uint32_t>(nslices(B) - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  finish_row(a, r, sm, h, scratch, T12);
 }
 
 }  // namespace
 
-cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, uint32_t *hist1_to_clear,
-                                cudaStream_t stream) {
-  select_clear_kernel<<<a.R, 256, 0, stream>>>(a, row_bound, hist1_to_clear);
+cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, cudaStream_t stream) {
+  select_clear_kernel<<<a.R, 256, 0, stream>>>(a, row_bound);
   return cudaGetLastError();
 }
 
-cudaError_t launch_first_hist(const SelectArgs &a, uint32_t *hist1, cudaStream_t stream) {
+cudaError_t launch_hist12(const SelectArgs &a, const uint32_t *coarse, cudaStream_t stream) {
   const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
-  first_hist_kernel<<<dim3(ns, a.R), kSelThreads, 0, stream>>>(a, hist1);
+  hist12_kernel<<<dim3(ns, a.R), kHistThreads, 0, stream>>>(a, coarse);
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const SelectArgs &a, cudaStream_t stream) {
+cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream) {
   static bool configured = false;
-  const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
-  hist2_kernel<<<dim3(ns, a.R), kSelThreads, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  collect_kernel<<<dim3(ns, a.R), kSelThreads, 0, stream>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int smem = kFinishCap * static_cast<int>(sizeof(unsigned long long));
   if (!configured) {
-    e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  finish_kernel<<<a.R, kFinishThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ns, a.R);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kFinishSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, collect_kernel, a);
 }
 
 }  // namespace idx
