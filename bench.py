@@ -41,7 +41,7 @@ METRIC = "µs per indexer launch and key·rows/s at 512K keys; % of HBM/FP8 roof
 WORKLOAD = ("cfg3: 2 requests x 4 rows, 524,288 keys each (page 64, shuffled pages), FP8 E4M3 cache "
             "with per-token scale, sigma 1/4 mixture keys, bf16 q, fp32 w, top-k 2048")
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_LAUNCH = 3  # prep, score, collect (with the per-row finish)
+KERNELS_PER_LAUNCH = 4  # prep, score, collect, finish
 
 
 def measured_peaks():

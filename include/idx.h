@@ -103,7 +103,9 @@ idx_status idx_score(const idx_problem *problem, float *scores, int64_t ld, uint
  *   row_bound  device int32 [R]; max_bound (host) >= every row_bound[r], ld >= max_bound.
  *   K          1 .. IDX_MAX_K.
  *   hist       device uint32 [R][64] first-digit histogram of these scores (as idx_score
- *              writes it) or NULL, in which case it is computed here.
+ *              writes it) or NULL.  Accepted for callers that hold one; this build
+ *              counts the finer 12-bit prefix of the radix keys in one pass over the
+ *              scores and does not need it.
  *   out_idx    device int32 [R][K]: positions ordered by score descending, then position
  *              ascending; entries past min(K, row_bound[r]) are -1.  Scores compare by value
  *              (-0.0 == +0.0).

@@ -26,7 +26,7 @@ cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 std::mutex g_mu;
 
 struct Layout {
-  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, rowsel, win, tie, scores;
+  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, cursor, rowsel, win, tie, scores;
   size_t total;
   int64_t scores_ld;
 };
@@ -47,6 +47,7 @@ Layout make_layout(int64_t R, int64_t K, int64_t max_bound, bool with_scores) {
   L.qop1 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
   L.wq = take(static_cast<size_t>(R) * idx::kHeads * 4);
   L.hist12 = take(static_cast<size_t>(R) * idx::kHistBins * 4);
+  L.cursor = take(static_cast<size_t>(R) * idx::kHistBins * 4);
   L.rowsel = take(static_cast<size_t>(R) * sizeof(idx::RowSelect));
   L.win = take(static_cast<size_t>(R) * K * 8);
   L.tie = take(static_cast<size_t>(R) * idx::kTieCap * 8);
@@ -67,6 +68,7 @@ Workspace carve(void *base, const Layout &L) {
   w.qop1 = b + L.qop1;
   w.wq = reinterpret_cast<float *>(b + L.wq);
   w.hist12 = reinterpret_cast<uint32_t *>(b + L.hist12);
+  w.cursor = reinterpret_cast<uint32_t *>(b + L.cursor);
   w.rowsel = reinterpret_cast<idx::RowSelect *>(b + L.rowsel);
   w.win = reinterpret_cast<unsigned long long *>(b + L.win);
   w.tie = reinterpret_cast<unsigned long long *>(b + L.tie);
@@ -242,7 +244,7 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
   a.ws = w;
   st = cuda_ok(idx::launch_select_clear(a, row_bound, s));
   if (st != IDX_OK) return st;
-  st = cuda_ok(idx::launch_hist12(a, hist, s));
+  st = cuda_ok(idx::launch_hist12(a, s));
   if (st != IDX_OK) return st;
   return cuda_ok(idx::launch_collect(a, s));
 }

@@ -42,10 +42,8 @@ struct PlanHeader {
 };
 
 struct RowSelect {       // per-row selection state
-  uint32_t nslices_done; // arrivals of the collect kernel's slices
-  uint32_t win_count;    // keys above the threshold bin, appended by the collect kernel
   uint32_t tie_count;    // keys in the threshold bin, appended by the collect kernel
-  uint32_t pad[5];
+  uint32_t pad[7];
 };
 
 // The fused score histogram counts the top kHistBits bits of radix_key(score):
@@ -62,8 +60,9 @@ struct Workspace {
   uint8_t *qop1;           // [R][8192]  FP8: q_lo; bf16: dims 64..127
   float *wq;               // [R][64]    weights / 2 with the query prescale folded in
   uint32_t *hist12;        // [R][4096]  12-bit histogram of the radix keys
+  uint32_t *cursor;        // [R][4096]  keys placed so far per 12-bit bin
   RowSelect *rowsel;       // [R]
-  unsigned long long *win; // [R][K]     keys above the threshold bin (composite keys)
+  unsigned long long *win; // [R][K]     keys above the threshold bin, grouped by bin (composite keys)
   unsigned long long *tie; // [R][kTieCap] keys in the threshold bin
   float *scores;           // [R][ld]    score scratch of idx_launch (else unused)
   int64_t scores_ld;
@@ -178,6 +177,17 @@ __device__ __forceinline__ void grid_dependency_wait() {
 // Lets the dependent grid be scheduled once every CTA of this grid has called it.
 __device__ __forceinline__ void grid_dependency_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), completing on an mbarrier
+// through cp_async_arrive_noinc.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed; the
+// barrier's expected count must include this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {

@@ -45,10 +45,9 @@ cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
 cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
                          cudaStream_t stream);
 // Selection.  idx_topk: clear the state and copy the bounds, build the 12-bit
-// histogram of the given scores (from the first-digit histogram `coarse` when
-// given).  Both paths end in the collect launch (with the per-row finish).
+// histogram of the given scores.  Both paths end in the collect and finish launches.
 cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, cudaStream_t stream);
-cudaError_t launch_hist12(const SelectArgs &a, const uint32_t *coarse, cudaStream_t stream);
+cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream);
 
 }  // namespace idx

@@ -212,7 +212,10 @@ __device__ void prep_row(const PrepArgs &a, int r) {
 __device__ void clear_row_state(const PrepArgs &a, int r) {
   const Workspace &ws = a.ws;
   if (a.hist_target != nullptr && threadIdx.x < 64) a.hist_target[r * 64 + threadIdx.x] = 0u;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+    ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+    if (a.clear_select) ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+  }
   if (a.clear_select && threadIdx.x < sizeof(RowSelect) / 4)
     reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
 }

@@ -16,8 +16,9 @@
 //     D[key][row*64 + head] = <k_key, q_row_head>      (M = 128, N = 64 * rows)
 // so a TMEM lane holds one key and each epilogue thread reduces its key's 64
 // head values of a row in registers.
-//   warp 0      producer: page ids, TMA of the key pages into an smem ring, the
-//               keys' scales into a second ring, and the group's query operand
+//   warp 0      producer: page ids (32 per lane load, a block ahead), TMA of the
+//               key pages into an smem ring, the keys' scales into a second ring
+//               (cp.async by the warp's lanes), and the group's query operand
 //               (bulk copy) on group changes;
 //   warp 1      MMA issuer (one thread) and TMEM owner; two accumulators in TMEM,
 //               so the MMA of tile k+1 runs while tile k's epilogue reads;
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       mbar_init(&bars->empty[s], 1);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
-      mbar_init(&bars->sfull[s], 1);
+      mbar_init(&bars->sfull[s], 32);          // one cp.async arrival per producer lane
       mbar_init(&bars->sempty[s], kEpiWarps);
     }
     for (int s = 0; s < 2; ++s) {
@@ -213,76 +214,82 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = l2_evict_first_policy();
-      GroupCursor cur;
-      cur.seek(ws.groups, num_groups, static_cast<int>(t0));
-      int cur_g = -1, req = 0, L = 0, nswitch = 0, tile_begin = 0;
-      // page ids of a tile: the pages of positions j*128 and j*128 + 64, or -1 past L
-      auto tile_pages = [&](int j, int32_t (&p)[2]) {
-        for (int h = 0; h < 2; ++h) {
-          const int64_t first = static_cast<int64_t>(j) * kTileKeys + h * kPage;
-          p[h] = first < L ? a.page_table[static_cast<int64_t>(req) * a.pt_stride + first / kPage] : -2;
+    // The whole warp runs the loop: lanes hold the page ids of the current and
+    // next block of 16 tiles (32 pages, one lane each) and copy the tile's 128
+    // key scales (16 bytes per lane); lane 0 issues the key pages' TMA.
+    const uint64_t policy = l2_evict_first_policy();
+    GroupCursor cur;
+    cur.seek(ws.groups, num_groups, static_cast<int>(t0));
+    int cur_g = -1, req = 0, L = 0, nswitch = 0, tile_begin = 0;
+    int32_t blk_ids = -2, nxt_ids = -2;   // this lane's page id in the current / next block
+    int blk = -1;                          // current block of 16 tiles within the group
+    // Waits are taken by lane 0 and the outcome broadcast, so the lanes never split.
+    auto warp_wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar, parity, limit, abort);
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+    auto block_ids = [&](int b) -> int32_t {
+      const int64_t page = static_cast<int64_t>(b) * 32 + lane;
+      return page * kPage < L ? a.page_table[static_cast<int64_t>(req) * a.pt_stride + page] : -2;
+    };
+    int k = 0;
+    for (int64_t t = t0; t < t1; ++t, ++k) {
+      if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
+        const Group grp = ws.groups[cur.g];
+        if (cur_g >= 0 && !warp_wait(&bars->bfree, (nswitch - 1) & 1)) {
+          if (lane == 0) set_abort(bars, ws.status);
+          break;
         }
-      };
-      int32_t next_pages[2] = {-2, -2};
-      int k = 0;
-      for (int64_t t = t0; t < t1; ++t, ++k) {
-        bool fresh = false;
-        if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
-          const Group grp = ws.groups[cur.g];
-          if (cur_g >= 0 && !mbar_wait(&bars->bfree, (nswitch - 1) & 1, limit, abort)) {
-            set_abort(bars, ws.status);
-            break;
-          }
+        if (lane == 0) {
           const uint32_t bytes = grp.nrows * kRowOperandBytes;
           mbar_arrive_expect_tx(&bars->bfull, 2 * bytes);
           bulk_load(sB0, ws.qop0 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
           bulk_load(sB1, ws.qop1 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
-          cur_g = cur.g;
-          req = grp.req;
-          L = grp.L;
-          tile_begin = grp.tile_begin;
-          ++nswitch;
-          fresh = true;
         }
-        const int j = static_cast<int>(t) - tile_begin;
-        int32_t pages[2];
-        if (fresh) {
-          tile_pages(j, pages);
+        cur_g = cur.g;
+        req = grp.req;
+        L = grp.L;
+        tile_begin = grp.tile_begin;
+        ++nswitch;
+        blk = (static_cast<int>(t) - tile_begin) >> 4;
+        blk_ids = block_ids(blk);
+        nxt_ids = block_ids(blk + 1);
+      }
+      const int j = static_cast<int>(t) - tile_begin;
+      if ((j >> 4) != blk) {               // next block: its ids were loaded a block ago
+        blk = j >> 4;
+        blk_ids = nxt_ids;
+        nxt_ids = block_ids(blk + 1);
+      }
+      int32_t pages[2];
+      pages[0] = __shfl_sync(0xffffffffu, blk_ids, (j & 15) * 2);
+      pages[1] = __shfl_sync(0xffffffffu, blk_ids, (j & 15) * 2 + 1);
+      const int s = k % C::kStages;
+      const int ss = k % kScaleSlots;
+      if (!warp_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1) ||
+          (KV == IDX_KV_E4M3 && !warp_wait(&bars->sempty[ss], ((k / kScaleSlots) & 1) ^ 1))) {
+        if (lane == 0) set_abort(bars, ws.status);
+        break;
+      }
+      uint32_t bytes = 0;
+      for (int h = 0; h < 2; ++h) {
+        if (pages[h] == -2) {
+          pages[h] = -1;
+        } else if (pages[h] >= 0 && pages[h] < a.P) {
+          bytes += C::kPageBytes;
         } else {
-          pages[0] = next_pages[0];
-          pages[1] = next_pages[1];
+          pages[h] = -1;
+          if (lane == 0) flag_status(ws.status, kStatusBadPage);
         }
-        // the next tile's page ids load while this tile waits for its slot
-        if (t + 1 < t1 && static_cast<int>(t) + 1 < cur.next_begin) tile_pages(j + 1, next_pages);
-        const int s = k % C::kStages;
-        const int ss = k % kScaleSlots;
-        if (!mbar_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1, limit, abort) ||
-            (KV == IDX_KV_E4M3 && !mbar_wait(&bars->sempty[ss], ((k / kScaleSlots) & 1) ^ 1, limit, abort))) {
-          set_abort(bars, ws.status);
-          break;
-        }
-        uint32_t bytes = 0;
-        for (int h = 0; h < 2; ++h) {
-          if (pages[h] == -2) {
-            pages[h] = -1;
-          } else if (pages[h] >= 0 && pages[h] < a.P) {
-            bytes += C::kPageBytes;
-          } else {
-            pages[h] = -1;
-            flag_status(ws.status, kStatusBadPage);
-          }
-        }
+      }
+      uint8_t *dst = sA + s * C::kStageBytes;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars->full[s], bytes);
-        if (KV == IDX_KV_E4M3) mbar_arrive_expect_tx(&bars->sfull[ss], (bytes / C::kPageBytes) * (kPage * 4));
-        uint8_t *dst = sA + s * C::kStageBytes;
         for (int h = 0; h < 2; ++h) {
           if (pages[h] < 0) continue;
           if (KV == IDX_KV_E4M3) {
             tma_load_2d(dst + h * (kPage * kDim), &kmap, 0, pages[h] * kPage, &bars->full[s], policy);
-            bulk_load(sscale + ss * kTileKeys + h * kPage, a.k_scale + static_cast<int64_t>(pages[h]) * kPage,
-                      kPage * 4, &bars->sfull[ss]);
           } else {
             tma_load_2d(dst + h * (kPage * 128), &kmap, 0, pages[h] * kPage, &bars->full[s], policy);
             tma_load_2d(dst + kTileKeys * 128 + h * (kPage * 128), &kmap, 64, pages[h] * kPage, &bars->full[s],
@@ -290,24 +297,32 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           }
         }
       }
-      // Wait for every copy still in flight before the CTA may exit (also after an abort).
-      int never = 0;
-      const int issued = k;
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last_use = issued - 1 - ((issued - 1 - s) % C::kStages);
-        if (!mbar_wait(&bars->full[s], (last_use / C::kStages) & 1, limit, &never))
-          flag_status(ws.status, kStatusTimeout);
-      }
       if (KV == IDX_KV_E4M3) {
-        for (int s = 0; s < kScaleSlots && s < issued; ++s) {
-          const int last_use = issued - 1 - ((issued - 1 - s) % kScaleSlots);
-          if (!mbar_wait(&bars->sfull[s], (last_use / kScaleSlots) & 1, limit, &never))
-            flag_status(ws.status, kStatusTimeout);
-        }
+        // lanes 0-15 copy page 0's 64 scales, lanes 16-31 page 1's, 16 bytes each
+        const int h = lane >> 4;
+        if (pages[h] >= 0)
+          cp_async16(sscale + ss * kTileKeys + lane * 4,
+                     a.k_scale + static_cast<int64_t>(pages[h]) * kPage + (lane & 15) * 4);
+        cp_async_arrive_noinc(&bars->sfull[ss]);
       }
-      if (nswitch > 0 && !mbar_wait(&bars->bfull, (nswitch - 1) & 1, limit, &never))
+    }
+    // Wait for every copy still in flight before the CTA may exit (also after an abort).
+    int never = 0;
+    const int issued = k;
+    for (int s = 0; s < C::kStages && s < issued; ++s) {
+      const int last_use = issued - 1 - ((issued - 1 - s) % C::kStages);
+      if (!mbar_wait(&bars->full[s], (last_use / C::kStages) & 1, limit, &never) && lane == 0)
         flag_status(ws.status, kStatusTimeout);
     }
+    if (KV == IDX_KV_E4M3) {
+      for (int s = 0; s < kScaleSlots && s < issued; ++s) {
+        const int last_use = issued - 1 - ((issued - 1 - s) % kScaleSlots);
+        if (!mbar_wait(&bars->sfull[s], (last_use / kScaleSlots) & 1, limit, &never) && lane == 0)
+          flag_status(ws.status, kStatusTimeout);
+      }
+    }
+    if (nswitch > 0 && !mbar_wait(&bars->bfull, (nswitch - 1) & 1, limit, &never) && lane == 0)
+      flag_status(ws.status, kStatusTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -480,10 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       if (mine) {
         const bool keep = valid && pos < bnd;
         if (keep) a.scores[static_cast<int64_t>(grp.row0 + set) * a.ld + pos] = score;
-        const uint32_t bin = keep ? (radix_key(score) >> (32 - kHistBits)) : 0xFFFFFFFFu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (keep && lane == __ffs(peers) - 1)
-          atomicAdd(&h[bin >> 1], static_cast<uint32_t>(__popc(peers)) << ((bin & 1) * 16));
+        const uint32_t bin = radix_key(score) >> (32 - kHistBits);
+        if (keep) atomicAdd(&h[bin >> 1], 1u << ((bin & 1) * 16));   // shared-memory atomics resolve collisions
       }
     }
     if (ok && cur_g >= 0) flush();

@@ -11,31 +11,35 @@
 // ascending.  The top K composites are exactly the wanted set, so ties at the
 // k-th value go to the lowest positions.
 //
-// Data flow (one row; many rows run side by side):
-//   hist12   the histogram of the top 12 bits of radix_key (the scoring kernel
-//            fuses it; idx_topk on given scores builds it with hist12_kernel,
-//            needing only the 64-bin first digit when that is given).
-//   collect  (slices of kSlice keys, one CTA each) finds the 12-bit bin T that
-//            holds the k-th key, appends every key above T (the winners, fewer
-//            than K) and every key in T (the candidates).  The CTA that finishes
-//            last for its row (an arrival counter: nothing waits) then
-//   finish   picks the K - winners best candidates by a radix select over the
-//            remaining 52 composite bits in shared memory, sorts the K keys and
-//            writes the positions, -1 past min(K, bound).  A row with more
-//            candidates than the buffer holds (thousands of equal scores) is
-//            resolved digit by digit over the row's scores instead.
+// The 12-bit histogram of the radix keys (fused into the scoring kernel; built
+// by hist12_kernel when idx_topk gets bare scores) gives, for every 12-bit bin,
+// the number of keys in higher bins: its exclusive prefix from the top.  The bin
+// T holding the k-th key is where that prefix crosses K, and every key in a
+// higher bin b belongs at output slots [prefix(b), prefix(b) + count(b)).
+//   collect  one CTA per slice of kSlice keys of a row: each key above T is
+//            written straight into its bin's slots (a per-bin cursor orders keys
+//            within the bin arbitrarily); each key in T is appended to the row's
+//            candidate list.
+//   finish   kParts CTAs per row sort the winners' bin-aligned segments in place
+//            (bins are contiguous ranges of slots, so segments sort
+//            independently); one more CTA per row picks the K - prefix(T) best
+//            candidates by radix digits of their remaining 52 bits, sorts them
+//            into the slots after the winners and writes -1 past min(K, bound).
+//            A row with more candidates than the list holds (thousands of equal
+//            scores) is resolved digit by digit over the row's scores instead.
 #include "idx_device.cuh"
 #include "launch.h"
 
 namespace idx {
 namespace {
 
-constexpr int kSlice = 16384;
-constexpr int kThreads = 1024;
-constexpr int kHistThreads = 512;
-constexpr int kSortCap = 2048;            // = IDX_MAX_K, power of two
-// dynamic shared memory of the collect/finish kernel
-constexpr int kFinishSmem = (kTieCap + kSortCap) * 8;
+constexpr int kSlice = 8192;
+constexpr int kThreads = 512;
+constexpr int kPer = kSlice / kThreads;
+constexpr int kParts = 4;                 // winner segments per row
+constexpr int kSortCap = IDX_MAX_K;       // power of two
+constexpr int kFinishSmem = kTieCap * 8;  // candidates (the sort buffer reuses the front)
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t pos) {
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
@@ -43,24 +47,10 @@ __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t po
 
 __device__ __forceinline__ int nslices(int32_t bound) { return bound > 0 ? (bound + kSlice - 1) / kSlice : 1; }
 
-// Among nbins bins taken in descending bin order, the bin holding the need-th key:
-// above < need <= above + hist[bin], above = keys in higher bins.  Block-wide:
-// every thread must call it and every thread gets the result.
-__device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_t *out_bin, uint32_t *out_above,
-                         uint32_t *scratch /* >= 34 words of shared memory */) {
-  const int per = (nbins + blockDim.x - 1) / blockDim.x;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    scratch[32] = 0u;
-    scratch[33] = 0u;
-  }
-  uint32_t sum = 0;
-  for (int m = 0; m < per; ++m) {
-    const int i = tid * per + m;
-    if (i < nbins) sum += hist[nbins - 1 - i];
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = sum;
+// Block-wide exclusive scan of v (every thread must call).
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t *scratch /* 33 */, uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
@@ -78,8 +68,29 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
     scratch[lane] = x;
   }
   __syncthreads();
-  const uint32_t excl = incl - sum + (warp > 0 ? scratch[warp - 1] : 0u);
+  const uint32_t excl = incl - v + (warp > 0 ? scratch[warp - 1] : 0u);
+  *total = scratch[(blockDim.x >> 5) - 1];
   __syncthreads();
+  return excl;
+}
+
+// Among nbins bins taken in descending bin order, the bin holding the need-th key:
+// above < need <= above + hist[bin], above = keys in higher bins.  Block-wide.
+__device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_t *out_bin, uint32_t *out_above,
+                         uint32_t *scratch /* >= 36 words */) {
+  const int per = (nbins + blockDim.x - 1) / blockDim.x;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    scratch[34] = 0u;
+    scratch[35] = 0u;
+  }
+  uint32_t sum = 0;
+  for (int m = 0; m < per; ++m) {
+    const int i = tid * per + m;
+    if (i < nbins) sum += hist[nbins - 1 - i];
+  }
+  uint32_t total;
+  const uint32_t excl = block_excl_scan(sum, scratch, &total);
   if (excl < need && need <= excl + sum) {
     uint32_t above = excl;
     for (int m = 0; m < per; ++m) {
@@ -87,16 +98,52 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
       if (i >= nbins) break;
       const uint32_t c = hist[nbins - 1 - i];
       if (above + c >= need) {
-        scratch[32] = static_cast<uint32_t>(nbins - 1 - i);
-        scratch[33] = above;
+        scratch[34] = static_cast<uint32_t>(nbins - 1 - i);
+        scratch[35] = above;
         break;
       }
       above += c;
     }
   }
   __syncthreads();
-  *out_bin = scratch[32];
-  *out_above = scratch[33];
+  *out_bin = scratch[34];
+  *out_above = scratch[35];
+  __syncthreads();
+}
+
+// The row's 12-bit bin layout: off[b] = keys in bins above b (into shared
+// memory), the threshold bin T (kNoBin when the row keeps all its keys) and the
+// number of keys above T.  Block-wide.
+__device__ void row_layout(const uint32_t *hist_g, int32_t B, int K, uint32_t *off, uint32_t *scratch,
+                           uint32_t *T, uint32_t *above) {
+  constexpr int per = kHistBins / kThreads;
+  uint32_t c[per];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int m = 0; m < per; ++m) {          // this thread's bins, highest first
+    c[m] = __ldcg(&hist_g[kHistBins - 1 - (threadIdx.x * per + m)]);
+    sum += c[m];
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan(sum, scratch, &total);
+  if (threadIdx.x == 0) {
+    scratch[34] = kNoBin;
+    scratch[35] = static_cast<uint32_t>(max(B, 0));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < per; ++m) {
+    const int b = kHistBins - 1 - (threadIdx.x * per + m);
+    off[b] = run;
+    if (B > K && run < static_cast<uint32_t>(K) && static_cast<uint32_t>(K) <= run + c[m]) {
+      scratch[34] = static_cast<uint32_t>(b);
+      scratch[35] = run;
+    }
+    run += c[m];
+  }
+  __syncthreads();
+  *T = scratch[34];
+  *above = scratch[35];
   __syncthreads();
 }
 
@@ -104,7 +151,10 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
 __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound) {
   const int r = blockIdx.x;
   const Workspace &ws = a.ws;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+    ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+    ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
+  }
   if (threadIdx.x < sizeof(RowSelect) / 4) reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     const int32_t b = row_bound[r];
@@ -114,38 +164,21 @@ __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound
   }
 }
 
-// The 12-bit histogram of given scores.  With a first-digit histogram `coarse`,
-// only the keys of the first digit that holds the k-th key are counted finely;
-// every other digit's count goes to that digit's lowest 12-bit bin, which keeps
-// every count "above" a bin exact for the threshold search.
-__global__ void __launch_bounds__(kHistThreads) hist12_kernel(const SelectArgs a, const uint32_t *coarse) {
+// The 12-bit histogram of given scores (one slice of a row per CTA).
+__global__ void __launch_bounds__(kThreads) hist12_kernel(const SelectArgs a) {
   __shared__ uint32_t h[kHistBins];
-  __shared__ uint32_t scratch[34];
   const int r = blockIdx.y;
   const int32_t B = a.bound[r];
-  if (B <= a.K || static_cast<int>(blockIdx.x) >= nslices(B)) return;   // rows that keep all keys skip it
-  const Workspace &ws = a.ws;
-  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads) h[i] = 0u;
-  uint32_t d1 = 0xFFFFFFFFu;
-  if (coarse != nullptr) {
-    __syncthreads();
-    uint32_t bin, above;
-    find_bin(coarse + r * 64, 64, static_cast<uint32_t>(a.K), &bin, &above, scratch);
-    d1 = bin;
-    if (blockIdx.x == 0 && threadIdx.x < 64 && threadIdx.x != d1 && coarse[r * 64 + threadIdx.x])
-      atomicAdd(&ws.hist12[static_cast<int64_t>(r) * kHistBins + threadIdx.x * 64], coarse[r * 64 + threadIdx.x]);
-  }
+  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads) h[i] = 0u;
   __syncthreads();
   const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
   const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
   const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  for (int64_t pos = begin + threadIdx.x; pos < end; pos += kHistThreads) {
-    const uint32_t key = radix_key(row[pos]);
-    if (d1 == 0xFFFFFFFFu || (key >> 26) == d1) atomicAdd(&h[key >> 20], 1u);
-  }
+  for (int64_t pos = begin + threadIdx.x; pos < end; pos += kThreads) atomicAdd(&h[radix_key(row[pos]) >> 20], 1u);
   __syncthreads();
-  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads)
-    if (h[i]) atomicAdd(&ws.hist12[static_cast<int64_t>(r) * kHistBins + i], h[i]);
+  for (int i = threadIdx.x; i < kHistBins; i += kThreads)
+    if (h[i]) atomicAdd(&a.ws.hist12[static_cast<int64_t>(r) * kHistBins + i], h[i]);
 }
 
 // ---------------------------------------------------------------------------- collect
@@ -162,10 +195,50 @@ __device__ __forceinline__ void warp_append(bool take, unsigned long long value,
   if (take && idx < cap) dst[idx] = value;
 }
 
-// Bitonic sort, descending, of n (a power of two) keys in shared memory.
-// Stages whose pairs stay inside one warp's 64-key block need only __syncwarp.
+__global__ void __launch_bounds__(kThreads) collect_kernel(const SelectArgs a) {
+  __shared__ uint32_t off[kHistBins];
+  __shared__ uint32_t scratch[36];
+  grid_dependency_wait();   // scores and the histogram come from the previous launch
+  const int r = blockIdx.y;
+  const int32_t B = a.bound[r];
+  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
+  const Workspace &ws = a.ws;
+  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
+  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
+  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
+  float sv[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {   // this thread's loads in flight while the layout is worked out
+    const int64_t pos = begin + i * kThreads + threadIdx.x;
+    sv[i] = pos < end ? __ldcg(row + pos) : 0.f;
+  }
+  uint32_t T, above;
+  row_layout(ws.hist12 + static_cast<int64_t>(r) * kHistBins, B, a.K, off, scratch, &T, &above);
+  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
+  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
+  uint32_t *cursor = ws.cursor + static_cast<int64_t>(r) * kHistBins;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int64_t pos = begin + i * kThreads + threadIdx.x;
+    const bool in = pos < end;
+    const uint32_t key = radix_key(sv[i]);
+    const uint32_t bin = key >> 20;
+    const unsigned long long c = composite(key, pos);
+    if (in && (T == kNoBin || bin > T)) {
+      const uint32_t slot = off[bin] + atomicAdd(&cursor[bin], 1u);
+      if (slot < static_cast<uint32_t>(a.K)) win[slot] = c;
+    }
+    warp_append(in && T != kNoBin && bin == T, c, tie, &ws.rowsel[r].tie_count, static_cast<uint32_t>(kTieCap));
+  }
+}
+
+// ---------------------------------------------------------------------------- finish
+// Bitonic sort, descending, of n (a power of two) keys in shared memory.  When
+// every pair of a stage lies in the 64-key block of the warp that handles it
+// (strides below 32, one pair per thread) the stage needs only __syncwarp.
 __device__ void bitonic_sort_desc(unsigned long long *s, int n) {
   const int half = n >> 1;
+  const bool one_pair = half <= static_cast<int>(blockDim.x);
   for (int size = 2; size <= n; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const int lg = __ffs(stride) - 1;
@@ -179,161 +252,160 @@ __device__ void bitonic_sort_desc(unsigned long long *s, int n) {
           s[hi] = x;
         }
       }
-      const int next = stride > 1 ? (stride >> 1) : (size << 1) >> 1;
-      if (stride >= 64 || next >= 64 || half > static_cast<int>(blockDim.x)) __syncthreads();
+      const int next = stride > 1 ? (stride >> 1) : size;
+      if (!one_pair || stride >= 32 || next >= 32) __syncthreads();
       else __syncwarp();
     }
   }
   __syncthreads();
 }
 
-// Digits of the low 52 composite bits, most significant first: six of 8 bits, one of 4.
-__device__ __forceinline__ int digit_shift(int d) { return d < 6 ? 44 - 8 * d : 0; }
-__device__ __forceinline__ int digit_width(int d) { return d < 6 ? 8 : 4; }
+__device__ __forceinline__ int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
 
-// Low 52 bits of a candidate's composite (the 12 high bits are the shared bin).
+// Digits of the low 52 composite bits, most significant first: two of 10 bits
+// (the score bits below the shared 12-bit bin) and three of 11, 11 and 10 bits
+// (the inverted position, for exact ties).
+__device__ __forceinline__ int digit_shift(int d) {
+  return d == 0 ? 42 : d == 1 ? 32 : d == 2 ? 21 : d == 3 ? 10 : 0;
+}
+__device__ __forceinline__ int digit_width(int d) { return d < 2 ? 10 : d < 4 ? 11 : 10; }
+
 __device__ __forceinline__ unsigned long long low52(unsigned long long c) { return c & ((1ull << 52) - 1); }
 
-// Picks the `need` largest of n candidates (composites sharing their top 12 bits)
-// by 8-bit digits of the low 52 bits; returns the smallest low-52 value taken.
-__device__ unsigned long long select_candidates(const unsigned long long *cand, int n, uint32_t need,
-                                                uint32_t *h /* 256 */, uint32_t *scratch) {
+// Threshold on the low 52 bits such that exactly `need` keys of the threshold
+// bin are >= it.  `candidate(i, valid)` yields the i-th key (valid = false to skip).
+template <typename Get>
+__device__ unsigned long long select_threshold(int64_t n, uint32_t need, Get candidate, uint32_t *h /* 2048 */,
+                                               uint32_t *scratch) {
   unsigned long long pre = 0ull;
-  for (int d = 0; d < 7; ++d) {
+  for (int d = 0; d < 5; ++d) {
     const int sh = digit_shift(d), wd = digit_width(d);
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
+    const int nb = 1 << wd;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) h[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned long long v = low52(cand[i]);
-      if (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd))) continue;
-      atomicAdd(&h[(v >> sh) & ((1u << wd) - 1u)], 1u);
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      bool valid;
+      const unsigned long long v = low52(candidate(i, valid));
+      if (!valid || (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd)))) continue;
+      atomicAdd(&h[(v >> sh) & (nb - 1u)], 1u);
     }
     __syncthreads();
     uint32_t bin, above;
-    find_bin(h, 1 << wd, need, &bin, &above, scratch);
+    find_bin(h, nb, need, &bin, &above, scratch);
+    const uint32_t cnt = h[bin];
     need -= above;
     pre |= static_cast<unsigned long long>(bin) << sh;
+    __syncthreads();
+    if (cnt == need) break;            // the whole bin is taken: the lower bits of pre stay 0
   }
   return pre;
 }
 
-__device__ void finish_row(const SelectArgs &a, int r, unsigned long long *sm, uint32_t *h, uint32_t *scratch,
-                           uint32_t T12) {
+__global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
+  extern __shared__ unsigned long long sm[];
+  __shared__ uint32_t off[kHistBins];
+  __shared__ uint32_t scratch[36];
+  __shared__ uint32_t bounds_s[2];
+  __shared__ uint32_t count_s;
+  grid_dependency_wait();   // every collect slice has placed its keys
+  const int part = blockIdx.x;
+  const int r = blockIdx.y;
   const Workspace &ws = a.ws;
   const int32_t B = a.bound[r];
   const int K = a.K;
-  const int nout = min(K, B);
-  unsigned long long *cand = sm;                 // kTieCap
-  unsigned long long *fin = sm + kTieCap;        // kSortCap
-  __shared__ uint32_t count_s;
-  const uint32_t nw = min(__ldcg(&ws.rowsel[r].win_count), static_cast<uint32_t>(kSortCap));
-  const uint32_t nt = B > K ? __ldcg(&ws.rowsel[r].tie_count) : 0u;
-  const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
-  const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-  for (uint32_t i = threadIdx.x; i < nw; i += blockDim.x) fin[i] = __ldcg(&win[i]);
-  if (threadIdx.x == 0) count_s = nw;
-  __syncthreads();
-  if (B > K) {
-    const uint32_t need = static_cast<uint32_t>(K) - nw;
-    if (nt <= static_cast<uint32_t>(kTieCap)) {
-      for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) cand[i] = __ldcg(&tie[i]);
-      __syncthreads();
-      const unsigned long long th = select_candidates(cand, static_cast<int>(nt), need, h, scratch);
-      for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) {
-        if (low52(cand[i]) >= th) {
-          const uint32_t at = atomicAdd(&count_s, 1u);
-          if (at < static_cast<uint32_t>(kSortCap)) fin[at] = cand[i];
-        }
-      }
-    } else {
-      // Too many keys in the threshold bin: the same digits, over the row's scores.
-      const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-      unsigned long long pre = 0ull;
-      uint32_t nd = need;
-      for (int d = 0; d < 7; ++d) {
-        const int sh = digit_shift(d), wd = digit_width(d);
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0u;
-        __syncthreads();
-        for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
-          const uint32_t key = radix_key(row[pos]);
-          if ((key >> 20) != T12) continue;
-          const unsigned long long v = low52(composite(key, pos));
-          if (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd))) continue;
-          atomicAdd(&h[(v >> sh) & ((1u << wd) - 1u)], 1u);
-        }
-        __syncthreads();
-        uint32_t bin, above;
-        find_bin(h, 1 << wd, nd, &bin, &above, scratch);
-        nd -= above;
-        pre |= static_cast<unsigned long long>(bin) << sh;
-      }
-      for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
-        const uint32_t key = radix_key(row[pos]);
-        if ((key >> 20) != T12) continue;
-        const unsigned long long c = composite(key, pos);
-        if (low52(c) >= pre) {
-          const uint32_t at = atomicAdd(&count_s, 1u);
-          if (at < static_cast<uint32_t>(kSortCap)) fin[at] = c;
-        }
+  const int nout = min(K, max(B, 0));
+  uint32_t T, above;
+  row_layout(ws.hist12 + static_cast<int64_t>(r) * kHistBins, B, K, off, scratch, &T, &above);
+  above = min(above, static_cast<uint32_t>(nout));
+  int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
+  unsigned long long *s = sm;
+
+  if (part < kParts) {
+    // This part's winner segment: from the first bin starting at or after
+    // part * S to the first bin starting at or after (part + 1) * S.
+    const uint32_t S = (above + kParts - 1) / kParts;
+    const uint32_t lo_cut = part * S, hi_cut = (part + 1) * S;
+    if (threadIdx.x == 0) {
+      bounds_s[0] = above;
+      bounds_s[1] = above;
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) {
+      if (T != kNoBin && static_cast<uint32_t>(b) <= T) continue;
+      const uint32_t o = off[b];
+      if (o >= above) continue;
+      if (o >= lo_cut) atomicMin(&bounds_s[0], o);
+      if (o >= hi_cut) atomicMin(&bounds_s[1], o);
+    }
+    __syncthreads();
+    const uint32_t s0 = bounds_s[0], s1 = max(bounds_s[0], bounds_s[1]);
+    const int n = static_cast<int>(s1 - s0);
+    if (n == 0) return;
+    const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
+    const int p2 = pow2_at_least(n);
+    for (int i = threadIdx.x; i < p2; i += blockDim.x) s[i] = i < n ? __ldcg(&win[s0 + i]) : 0ull;
+    __syncthreads();
+    bitonic_sort_desc(s, p2);
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      out[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(s[i] & 0xFFFFFFFFull));
+    return;
+  }
+
+  // The threshold bin's part: the `need` best candidates after the winners.
+  const uint32_t need = static_cast<uint32_t>(nout) - above;
+  for (int j = nout + threadIdx.x; j < K; j += blockDim.x) out[j] = -1;
+  if (need == 0) return;
+  const uint32_t nt = __ldcg(&ws.rowsel[r].tie_count);
+  unsigned long long *cand = sm;
+  if (threadIdx.x == 0) count_s = 0;
+  unsigned long long th;
+  if (nt <= static_cast<uint32_t>(kTieCap)) {
+    const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
+    for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) cand[i] = __ldcg(&tie[i]);
+    __syncthreads();
+    th = select_threshold(static_cast<int64_t>(nt), need,
+                          [&](int64_t i, bool &valid) { valid = true; return cand[i]; }, off, scratch);
+    // keep the chosen ones at the front (the threshold pass is done with cand)
+    __syncthreads();
+    unsigned long long mine[kTieCap / kThreads];
+    int nm = 0;
+    for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x)
+      if (low52(cand[i]) >= th) mine[nm++] = cand[i];
+    __syncthreads();
+    for (int m = 0; m < nm; ++m) cand[atomicAdd(&count_s, 1u)] = mine[m];
+  } else {
+    // Too many keys in the threshold bin for the list: the same digits, over the row.
+    const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
+    th = select_threshold(static_cast<int64_t>(B), need,
+                          [&](int64_t pos, bool &valid) {
+                            const uint32_t key = radix_key(row[pos]);
+                            valid = (key >> 20) == T;
+                            return composite(key, pos);
+                          },
+                          off, scratch);
+    __syncthreads();
+    for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
+      const uint32_t key = radix_key(row[pos]);
+      if ((key >> 20) != T) continue;
+      const unsigned long long c = composite(key, pos);
+      if (low52(c) >= th) {
+        const uint32_t at = atomicAdd(&count_s, 1u);
+        if (at < static_cast<uint32_t>(kSortCap)) cand[at] = c;
       }
     }
   }
   __syncthreads();
-  const int n = min(static_cast<int>(count_s), kSortCap);
-  int p2 = 1;
-  while (p2 < n) p2 <<= 1;
-  for (int i = n + threadIdx.x; i < p2; i += blockDim.x) fin[i] = 0ull;
+  const int n = min(static_cast<int>(count_s), static_cast<int>(need));
+  const int p2 = pow2_at_least(n);
+  for (int i = n + threadIdx.x; i < p2; i += blockDim.x) cand[i] = 0ull;
   __syncthreads();
-  bitonic_sort_desc(fin, p2);
-  int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
-  for (int j = threadIdx.x; j < K; j += blockDim.x)
-    out[j] = (j < nout && j < n) ? static_cast<int32_t>(~static_cast<uint32_t>(fin[j] & 0xFFFFFFFFull)) : -1;
-}
-
-__global__ void __launch_bounds__(kThreads) collect_kernel(const SelectArgs a) {
-  extern __shared__ unsigned long long sm[];
-  __shared__ uint32_t h[256];
-  __shared__ uint32_t hist_s[kHistBins];
-  __shared__ uint32_t scratch[34];
-  __shared__ int is_last;
-  grid_dependency_wait();   // scores and the histogram come from the previous launch
-  const int r = blockIdx.y;
-  const int32_t B = a.bound[r];
-  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
-  const Workspace &ws = a.ws;
-  const bool take_all = B <= a.K;
-  uint32_t T12 = 0;
-  if (!take_all) {
-    for (int i = threadIdx.x; i < kHistBins; i += kThreads)
-      hist_s[i] = __ldcg(&ws.hist12[static_cast<int64_t>(r) * kHistBins + i]);
-    __syncthreads();
-    uint32_t above;
-    find_bin(hist_s, kHistBins, static_cast<uint32_t>(a.K), &T12, &above, scratch);
-  }
-  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
-  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
-  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-  for (int64_t base = begin; base < end; base += kThreads) {
-    const int64_t pos = base + threadIdx.x;
-    const bool in = pos < end;
-    const uint32_t key = in ? radix_key(row[pos]) : 0u;
-    const uint32_t bin = key >> 20;
-    const bool w = in && (take_all || bin > T12);
-    const bool t = in && !take_all && bin == T12;
-    const unsigned long long c = composite(key, pos);
-    warp_append(w, c, win, &ws.rowsel[r].win_count, static_cast<uint32_t>(a.K));
-    warp_append(t, c, tie, &ws.rowsel[r].tie_count, static_cast<uint32_t>(kTieCap));
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0)
-    is_last = atomicAdd(&ws.rowsel[r].nslices_done, 1u) == static_cast<uint32_t>(nslices(B) - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  finish_row(a, r, sm, h, scratch, T12);
+  bitonic_sort_desc(cand, p2);
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    out[above + i] = static_cast<int32_t>(~static_cast<uint32_t>(cand[i] & 0xFFFFFFFFull));
 }
 
 }  // namespace
@@ -343,31 +415,39 @@ cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_hist12(const SelectArgs &a, const uint32_t *coarse, cudaStream_t stream) {
+cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream) {
   const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
-  hist12_kernel<<<dim3(ns, a.R), kHistThreads, 0, stream>>>(a, coarse);
+  hist12_kernel<<<dim3(ns, a.R), kThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmem);
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ns, a.R);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kFinishSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, collect_kernel, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, collect_kernel, a);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t fcfg = {};
+  fcfg.gridDim = dim3(kParts + 1, a.R);
+  fcfg.blockDim = dim3(kThreads);
+  fcfg.dynamicSmemBytes = kFinishSmem;
+  fcfg.stream = stream;
+  fcfg.attrs = attr;
+  fcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&fcfg, finish_kernel, a);
 }
 
 }  // namespace idx
