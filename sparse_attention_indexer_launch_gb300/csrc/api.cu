@@ -25,8 +25,13 @@ int64_t g_stall_next = 0;
 cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
 std::mutex g_mu;
 
+uint64_t wait_limit() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return static_cast<uint64_t>(g_wait_limit_ns);
+}
+
 struct Layout {
-  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, cursor, rowsel, win, tie, scores;
+  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, cursor, hist_sub, rowsel, win, tie, scores;
   size_t total;
   int64_t scores_ld;
 };
@@ -48,6 +53,7 @@ Layout make_layout(int64_t R, int64_t K, int64_t max_bound, bool with_scores) {
   L.wq = take(static_cast<size_t>(R) * idx::kHeads * 4);
   L.hist12 = take(static_cast<size_t>(R) * idx::kHistBins * 4);
   L.cursor = take(static_cast<size_t>(R) * idx::kHistBins * 4);
+  L.hist_sub = take(static_cast<size_t>(R) * idx::kSubBins * 4);
   L.rowsel = take(static_cast<size_t>(R) * sizeof(idx::RowSelect));
   L.win = take(static_cast<size_t>(R) * K * 8);
   L.tie = take(static_cast<size_t>(R) * idx::kTieCap * 8);
@@ -69,6 +75,7 @@ Workspace carve(void *base, const Layout &L) {
   w.wq = reinterpret_cast<float *>(b + L.wq);
   w.hist12 = reinterpret_cast<uint32_t *>(b + L.hist12);
   w.cursor = reinterpret_cast<uint32_t *>(b + L.cursor);
+  w.hist_sub = reinterpret_cast<uint32_t *>(b + L.hist_sub);
   w.rowsel = reinterpret_cast<idx::RowSelect *>(b + L.rowsel);
   w.win = reinterpret_cast<unsigned long long *>(b + L.win);
   w.tie = reinterpret_cast<unsigned long long *>(b + L.tie);
@@ -242,6 +249,8 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
   a.max_bound = max_bound;
   a.out_idx = out_idx;
   a.ws = w;
+  a.bulk_rows = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && ld % 4 == 0;
+  a.wait_limit_ns = wait_limit();
   st = cuda_ok(idx::launch_select_clear(a, row_bound, s));
   if (st != IDX_OK) return st;
   st = cuda_ok(idx::launch_hist12(a, s));
@@ -269,6 +278,8 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   a.max_bound = problem->max_bound;
   a.out_idx = out_idx;
   a.ws = w;
+  a.bulk_rows = (reinterpret_cast<uintptr_t>(w.scores) & 15u) == 0 && w.scores_ld % 4 == 0;
+  a.wait_limit_ns = wait_limit();
   return cuda_ok(idx::launch_collect(a, s));
 }
 

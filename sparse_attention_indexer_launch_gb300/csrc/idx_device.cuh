@@ -43,13 +43,17 @@ struct PlanHeader {
 
 struct RowSelect {       // per-row selection state
   uint32_t tie_count;    // keys in the threshold bin, appended by the collect kernel
-  uint32_t pad[7];
+  uint32_t T;            // 12-bit bin holding the k-th key (0xFFFFFFFF: the row keeps all keys)
+  uint32_t above;        // keys in higher bins (= the winners)
+  uint32_t pad;
+  uint32_t cut[8];       // winner slots cut into bin-aligned segments, one per finish part
 };
 
 // The fused score histogram counts the top kHistBits bits of radix_key(score):
 // its 64-bin marginal (top 6 bits) is the first digit radix_key >> 26.
 constexpr int kHistBits = 12;
 constexpr int kHistBins = 1 << kHistBits;
+constexpr int kSubBins = 1024;   // second digit of the threshold bin's keys (the next 10 bits)
 
 struct Workspace {
   uint32_t *status;        // [1]
@@ -61,6 +65,7 @@ struct Workspace {
   float *wq;               // [R][64]    weights / 2 with the query prescale folded in
   uint32_t *hist12;        // [R][4096]  12-bit histogram of the radix keys
   uint32_t *cursor;        // [R][4096]  keys placed so far per 12-bit bin
+  uint32_t *hist_sub;      // [R][1024]  second-digit histogram of the threshold bin
   RowSelect *rowsel;       // [R]
   unsigned long long *win; // [R][K]     keys above the threshold bin, grouped by bin (composite keys)
   unsigned long long *tie; // [R][kTieCap] keys in the threshold bin

@@ -39,6 +39,8 @@ struct SelectArgs {
   int32_t R, K, max_bound;
   int32_t *out_idx;        // [R][K]
   Workspace ws;
+  int32_t bulk_rows;       // scores and ld allow 16-byte bulk copies of row slices
+  uint64_t wait_limit_ns;
 };
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);

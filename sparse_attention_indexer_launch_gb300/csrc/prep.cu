@@ -216,6 +216,8 @@ __device__ void clear_row_state(const PrepArgs &a, int r) {
     ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
     if (a.clear_select) ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
   }
+  if (a.clear_select)
+    for (int i = threadIdx.x; i < kSubBins; i += blockDim.x) ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i] = 0u;
   if (a.clear_select && threadIdx.x < sizeof(RowSelect) / 4)
     reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
 }

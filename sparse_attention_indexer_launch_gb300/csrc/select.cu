@@ -16,17 +16,22 @@
 // the number of keys in higher bins: its exclusive prefix from the top.  The bin
 // T holding the k-th key is where that prefix crosses K, and every key in a
 // higher bin b belongs at output slots [prefix(b), prefix(b) + count(b)).
-//   collect  one CTA per slice of kSlice keys of a row: each key above T is
-//            written straight into its bin's slots (a per-bin cursor orders keys
-//            within the bin arbitrarily); each key in T is appended to the row's
-//            candidate list.
-//   finish   kParts CTAs per row sort the winners' bin-aligned segments in place
-//            (bins are contiguous ranges of slots, so segments sort
-//            independently); one more CTA per row picks the K - prefix(T) best
-//            candidates by radix digits of their remaining 52 bits, sorts them
-//            into the slots after the winners and writes -1 past min(K, bound).
-//            A row with more candidates than the list holds (thousands of equal
-//            scores) is resolved digit by digit over the row's scores instead.
+//   collect  one CTA per slice of kSlice keys of a row: the slice is copied to
+//            shared memory while the CTA scans the row's histogram for T and the
+//            prefixes.  Keys above T are listed, then written straight into
+//            their bin's slots (a per-bin cursor orders keys within the bin
+//            arbitrarily); keys in T are appended to the row's candidate list and
+//            counted in a 1024-bin histogram of their next 10 bits (the second
+//            digit).  The first slice also records T and the cuts of the winner
+//            slots into kParts bin-aligned segments.
+//   finish   kParts CTAs per row sort the winners' segments in place (bins are
+//            contiguous ranges of slots, so segments sort independently); one
+//            more CTA per row takes the candidates whose second digit is above
+//            the one holding the k-th key, picks the rest from that digit's bin by
+//            the remaining 42 bits, sorts them into the slots after the winners
+//            and writes -1 past min(K, bound).  A row with more candidates than
+//            the list holds (thousands of equal scores) is resolved digit by
+//            digit over the row's scores instead.
 #include "idx_device.cuh"
 #include "launch.h"
 
@@ -34,12 +39,23 @@ namespace idx {
 namespace {
 
 constexpr int kSlice = 8192;
-constexpr int kThreads = 512;
-constexpr int kPer = kSlice / kThreads;
-constexpr int kParts = 4;                 // winner segments per row
-constexpr int kSortCap = IDX_MAX_K;       // power of two
-constexpr int kFinishSmem = kTieCap * 8;  // candidates (the sort buffer reuses the front)
+constexpr int kCollectThreads = 256;
+constexpr int kWinList = IDX_MAX_K;        // winners of one slice (at most K)
+constexpr int kCandList = 4096;            // candidates of one slice kept in shared memory
+constexpr int kCollectSmem = kSlice * 4 + (kWinList + kCandList) * 2 + kHistBins * 2;
+constexpr int kThreads = 512;              // hist12 and finish
+constexpr int kParts = 4;                  // winner segments per row
+constexpr int kSortCap = IDX_MAX_K;        // power of two
+constexpr int kTilesPerWarp = kSortCap / 64 / (kThreads / 32);   // 64-key sort tiles per warp
+constexpr int kFinishSmem = (kTieCap + kSortCap) * 8 + 2 * 4096 * 4;   // candidates, the keys to sort, buckets
+// Requested by each finish CTA: more than half an SM's shared memory, so that the
+// scheduler gives every CTA an SM of its own instead of packing two on one.
+constexpr int kFinishSmemAlloc = 120 * 1024;
+static_assert(kFinishSmem <= kFinishSmemAlloc, "finish shared memory");
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+static_assert(kParts + 1 <= 8, "RowSelect holds the cuts");
+static_assert(kTilesPerWarp >= 1 && kSortCap % 64 == 0, "sort tiles");
+static_assert(kCollectSmem <= 54 * 1024, "four collect CTAs per SM");
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t pos) {
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
@@ -111,42 +127,6 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
   __syncthreads();
 }
 
-// The row's 12-bit bin layout: off[b] = keys in bins above b (into shared
-// memory), the threshold bin T (kNoBin when the row keeps all its keys) and the
-// number of keys above T.  Block-wide.
-__device__ void row_layout(const uint32_t *hist_g, int32_t B, int K, uint32_t *off, uint32_t *scratch,
-                           uint32_t *T, uint32_t *above) {
-  constexpr int per = kHistBins / kThreads;
-  uint32_t c[per];
-  uint32_t sum = 0;
-#pragma unroll
-  for (int m = 0; m < per; ++m) {          // this thread's bins, highest first
-    c[m] = __ldcg(&hist_g[kHistBins - 1 - (threadIdx.x * per + m)]);
-    sum += c[m];
-  }
-  uint32_t total;
-  uint32_t run = block_excl_scan(sum, scratch, &total);
-  if (threadIdx.x == 0) {
-    scratch[34] = kNoBin;
-    scratch[35] = static_cast<uint32_t>(max(B, 0));
-  }
-  __syncthreads();
-#pragma unroll
-  for (int m = 0; m < per; ++m) {
-    const int b = kHistBins - 1 - (threadIdx.x * per + m);
-    off[b] = run;
-    if (B > K && run < static_cast<uint32_t>(K) && static_cast<uint32_t>(K) <= run + c[m]) {
-      scratch[34] = static_cast<uint32_t>(b);
-      scratch[35] = run;
-    }
-    run += c[m];
-  }
-  __syncthreads();
-  *T = scratch[34];
-  *above = scratch[35];
-  __syncthreads();
-}
-
 // ---------------------------------------------------------------------------- idx_topk front
 __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound) {
   const int r = blockIdx.x;
@@ -155,6 +135,7 @@ __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound
     ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
     ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
   }
+  for (int i = threadIdx.x; i < kSubBins; i += blockDim.x) ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i] = 0u;
   if (threadIdx.x < sizeof(RowSelect) / 4) reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     const int32_t b = row_bound[r];
@@ -182,8 +163,9 @@ __global__ void __launch_bounds__(kThreads) hist12_kernel(const SelectArgs a) {
 }
 
 // ---------------------------------------------------------------------------- collect
-__device__ __forceinline__ void warp_append(bool take, unsigned long long value, unsigned long long *dst,
-                                            uint32_t *counter, uint32_t cap) {
+// Appends `take` lanes' values to list[] at slots counted by *counter (shared).
+__device__ __forceinline__ void warp_push(bool take, uint16_t value, uint16_t *list, uint32_t *counter,
+                                          uint32_t cap) {
   const uint32_t ballot = __ballot_sync(0xffffffffu, take);
   if (ballot == 0u) return;
   const int lane = threadIdx.x & 31;
@@ -191,77 +173,394 @@ __device__ __forceinline__ void warp_append(bool take, unsigned long long value,
   uint32_t base = 0;
   if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(ballot)));
   base = __shfl_sync(0xffffffffu, base, leader);
-  const uint32_t idx = base + __popc(ballot & ((1u << lane) - 1u));
-  if (take && idx < cap) dst[idx] = value;
+  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
+  if (take && at < cap) list[at] = value;
 }
 
-__global__ void __launch_bounds__(kThreads) collect_kernel(const SelectArgs a) {
-  __shared__ uint32_t off[kHistBins];
+__global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectArgs a) {
+  extern __shared__ __align__(128) unsigned char csm[];
+  float *vals = reinterpret_cast<float *>(csm);                               // [kSlice]
+  uint16_t *wlist = reinterpret_cast<uint16_t *>(csm + kSlice * 4);           // [kWinList]
+  uint16_t *clist = wlist + kWinList;                                         // [kCandList]
+  uint16_t *off = clist + kCandList;                                          // [kHistBins], winner bins only
+  __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t scratch[36];
-  grid_dependency_wait();   // scores and the histogram come from the previous launch
+  __shared__ uint32_t cuts[kParts + 1];
+  __shared__ uint32_t nwin, ncand;
+  __shared__ int abort_flag;
+
+  grid_dependency_wait();   // scores and histogram come from the previous launch
+  grid_dependency_trigger();
   const int r = blockIdx.y;
+  const int tid = threadIdx.x;
   const int32_t B = a.bound[r];
   if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
   const Workspace &ws = a.ws;
   const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
-  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  float sv[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {   // this thread's loads in flight while the layout is worked out
-    const int64_t pos = begin + i * kThreads + threadIdx.x;
-    sv[i] = pos < end ? __ldcg(row + pos) : 0.f;
-  }
-  uint32_t T, above;
-  row_layout(ws.hist12 + static_cast<int64_t>(r) * kHistBins, B, a.K, off, scratch, &T, &above);
-  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
-  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-  uint32_t *cursor = ws.cursor + static_cast<int64_t>(r) * kHistBins;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int64_t pos = begin + i * kThreads + threadIdx.x;
-    const bool in = pos < end;
-    const uint32_t key = radix_key(sv[i]);
-    const uint32_t bin = key >> 20;
-    const unsigned long long c = composite(key, pos);
-    if (in && (T == kNoBin || bin > T)) {
-      const uint32_t slot = off[bin] + atomicAdd(&cursor[bin], 1u);
-      if (slot < static_cast<uint32_t>(a.K)) win[slot] = c;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(B), begin + kSlice) - begin));
+  const float *src = a.scores + static_cast<int64_t>(r) * a.ld + begin;
+
+  // 1. the slice into shared memory (one bulk copy when the rows are 16-byte aligned)
+  const uint32_t bytes = (static_cast<uint32_t>(n) * 4u + 15u) & ~15u;
+  if (tid == 0) {
+    nwin = 0u;
+    ncand = 0u;
+    abort_flag = 0;
+    if (a.bulk_rows) {
+      mbar_init(&bar, 1);
+      fence_barrier_init();
+      mbar_arrive_expect_tx(&bar, bytes);
+      if (bytes > 0u) bulk_load(vals, src, bytes, &bar);
     }
-    warp_append(in && T != kNoBin && bin == T, c, tie, &ws.rowsel[r].tie_count, static_cast<uint32_t>(kTieCap));
+  }
+  if (!a.bulk_rows)
+    for (int i = tid; i < n; i += kCollectThreads) vals[i] = __ldcg(src + i);
+
+  // 2. meanwhile: the row's 12-bit layout (T, keys above T, the winner bins' slots).
+  //    The histogram is staged through shared memory (over the lists, which are not
+  //    in use yet) by coalesced loads; each thread then scans a run of `per` bins.
+  constexpr int per = kHistBins / kCollectThreads;
+  static_assert(per % 4 == 0 && kHistBins * 4 <= (kWinList + kCandList) * 2 + kHistBins * 2, "histogram staging");
+  uint32_t *hs = reinterpret_cast<uint32_t *>(wlist);
+  const uint4 *hg = reinterpret_cast<const uint4 *>(ws.hist12 + static_cast<int64_t>(r) * kHistBins);
+  for (int i = tid; i < kHistBins / 4; i += kCollectThreads) reinterpret_cast<uint4 *>(hs)[i] = __ldcg(&hg[i]);
+  __syncthreads();
+  uint32_t c[per];   // this thread's bins, highest first: bins 4095 - tid * per - m
+  uint32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < per / 4; ++k) {
+    const uint4 h4 = reinterpret_cast<const uint4 *>(hs + kHistBins - per * (tid + 1))[per / 4 - 1 - k];
+    c[4 * k] = h4.w;
+    c[4 * k + 1] = h4.z;
+    c[4 * k + 2] = h4.y;
+    c[4 * k + 3] = h4.x;
+  }
+#pragma unroll
+  for (int m = 0; m < per; ++m) sum += c[m];
+  uint32_t total;
+  uint32_t run = block_excl_scan(sum, scratch, &total);   // its barriers also end the reads of hs
+  if (tid == 0) {
+    scratch[34] = kNoBin;
+    scratch[35] = static_cast<uint32_t>(max(B, 0));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < per; ++m) {
+    const int b = kHistBins - 1 - (tid * per + m);
+    off[b] = static_cast<uint16_t>(min(run, 0xFFFFu));
+    if (B > a.K && run < static_cast<uint32_t>(a.K) && static_cast<uint32_t>(a.K) <= run + c[m]) {
+      scratch[34] = static_cast<uint32_t>(b);
+      scratch[35] = run;
+    }
+    run += c[m];
+  }
+  __syncthreads();
+  const uint32_t T = scratch[34];
+  const uint32_t above = min(scratch[35], static_cast<uint32_t>(min(a.K, max(B, 0))));
+
+  if (blockIdx.x == 0) {   // the finish kernel's segment cuts: first winner-bin start at or after p * S
+    const uint32_t S = (above + kParts - 1) / kParts;
+    if (tid <= kParts) cuts[tid] = above;
+    __syncthreads();
+    for (int b = tid; b < kHistBins; b += kCollectThreads) {
+      if (T != kNoBin && static_cast<uint32_t>(b) <= T) continue;
+      const uint32_t o = off[b];
+      if (o >= above) continue;
+      for (int p = 1; p < kParts; ++p)
+        if (o >= p * S) atomicMin(&cuts[p], o);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      RowSelect &rs = ws.rowsel[r];
+      rs.T = T;
+      rs.above = above;
+      uint32_t prev = 0u;
+      rs.cut[0] = 0u;
+      for (int p = 1; p <= kParts; ++p) {
+        prev = max(cuts[p], prev);
+        rs.cut[p] = prev;
+      }
+    }
+  }
+
+  // 3. classify the slice
+  if (a.bulk_rows) {
+    if (!mbar_wait(&bar, 0, a.wait_limit_ns, &abort_flag)) {
+      flag_status(ws.status, kStatusTimeout);
+      return;   // the copy's completion is not awaited further: the status reports the launch failed
+    }
+  } else {
+    __syncthreads();
+  }
+  {
+    // winners: bin > Tw; candidates: bin == Tc (Tw = Tc = -1 when the row keeps every key)
+    const int Tw = T == kNoBin ? -1 : static_cast<int>(T);
+    const int Tc = static_cast<int>(T);
+    const float4 *v4 = reinterpret_cast<const float4 *>(vals);
+#pragma unroll 2
+    for (int i = 0; i < kSlice / 4 / kCollectThreads; ++i) {
+      const int q = i * kCollectThreads + tid;
+      const float4 x = v4[q];
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+      uint32_t wm = 0u, cm = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int bin = static_cast<int>(radix_key(xs[e]) >> 20);
+        const bool in = 4 * q + e < n;
+        wm |= static_cast<uint32_t>(in && bin > Tw) << e;
+        cm |= static_cast<uint32_t>(in && bin == Tc) << e;
+      }
+      if (__any_sync(0xffffffffu, (wm | cm) != 0u)) {   // rare: most keys fall below T
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          warp_push((wm >> e) & 1u, static_cast<uint16_t>(4 * q + e), wlist, &nwin, kWinList);
+          warp_push((cm >> e) & 1u, static_cast<uint16_t>(4 * q + e), clist, &ncand, kCandList);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // 4. winners into their slots; candidates onto the row's list
+  const uint32_t nw = min(nwin, static_cast<uint32_t>(kWinList));
+  unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
+  uint32_t *cursor = ws.cursor + static_cast<int64_t>(r) * kHistBins;
+  for (uint32_t i = tid; i < nw; i += kCollectThreads) {
+    const int j = wlist[i];
+    const uint32_t key = radix_key(vals[j]);
+    const uint32_t bin = key >> 20;
+    const uint32_t slot = static_cast<uint32_t>(off[bin]) + atomicAdd(&cursor[bin], 1u);
+    if (slot < static_cast<uint32_t>(a.K)) win[slot] = composite(key, begin + j);
+  }
+  const uint32_t nc = ncand;
+  RowSelect &rs = ws.rowsel[r];
+  if (nc > static_cast<uint32_t>(kCandList)) {
+    // more candidates than one slice keeps: the finish resolves the row from its scores
+    if (tid == 0) atomicAdd(&rs.tie_count, static_cast<uint32_t>(kTieCap) + 1u);
+    return;
+  }
+  unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
+  uint32_t *hsub = ws.hist_sub + static_cast<int64_t>(r) * kSubBins;
+  const int lane = tid & 31;
+  for (uint32_t i0 = tid & ~31u; i0 < nc; i0 += kCollectThreads) {   // one warp per 32 candidates
+    const uint32_t i = i0 + lane;
+    const uint32_t cnt = min(32u, nc - i0);
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&rs.tie_count, cnt);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (i < nc) {
+      const int j = clist[i];
+      const uint32_t key = radix_key(vals[j]);
+      atomicAdd(&hsub[(key >> 10) & (kSubBins - 1)], 1u);
+      if (base + lane < static_cast<uint32_t>(kTieCap)) tie[base + lane] = composite(key, begin + j);
+    }
   }
 }
 
 // ---------------------------------------------------------------------------- finish
-// Bitonic sort, descending, of n (a power of two) keys in shared memory.  When
-// every pair of a stage lies in the 64-key block of the warp that handles it
-// (strides below 32, one pair per thread) the stage needs only __syncwarp.
-__device__ void bitonic_sort_desc(unsigned long long *s, int n) {
-  const int half = n >> 1;
-  const bool one_pair = half <= static_cast<int>(blockDim.x);
-  for (int size = 2; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const int lg = __ffs(stride) - 1;
-      for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const int lo = ((i >> lg) << (lg + 1)) | (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long x = s[lo], y = s[hi];
-        if ((x < y) == desc) {
-          s[lo] = y;
-          s[hi] = x;
-        }
+// Sorting n keys (n a power of two, 64 <= n <= kSortCap) in descending order:
+// every warp first sorts 64-key tiles in registers (lane l holds keys l and l + 32;
+// a bitonic network unrolled at compile time: in-thread swaps for stride 32,
+// shuffles below), then log2(n / 64) merge rounds double the sorted runs.  In a
+// round each key finds its place in the merged run by a binary search for its
+// rank in the partner run (equal keys: the left run's go first), so a round is
+// one pass and one barrier.
+template <int SIZE, int STRIDE>
+__device__ __forceinline__ void tile_stage(unsigned long long &a, unsigned long long &b, int lane) {
+  if constexpr (STRIDE == 32) {   // in-thread pair (l, l + 32); SIZE == 64 sorts the whole tile descending
+    const bool sw = a < b;
+    const unsigned long long x = a, y = b;
+    a = sw ? y : x;
+    b = sw ? x : y;
+  } else {
+    const bool lo = (lane & STRIDE) == 0;
+    const bool desc_a = (lane & SIZE) == 0;
+    const bool desc_b = ((lane + 32) & SIZE) == 0;
+    const unsigned long long ya = __shfl_xor_sync(0xffffffffu, a, STRIDE);
+    const unsigned long long yb = __shfl_xor_sync(0xffffffffu, b, STRIDE);
+    a = ((a < ya) == (lo == desc_a)) ? ya : a;
+    b = ((b < yb) == (lo == desc_b)) ? yb : b;
+  }
+}
+
+template <int SIZE, int STRIDE>
+__device__ __forceinline__ void tile_merge(unsigned long long &a, unsigned long long &b, int lane) {
+  tile_stage<SIZE, STRIDE>(a, b, lane);
+  if constexpr (STRIDE > 1) tile_merge<SIZE, STRIDE / 2>(a, b, lane);
+}
+
+template <int SIZE>
+__device__ __forceinline__ void tile_sort(unsigned long long &a, unsigned long long &b, int lane) {
+  tile_merge<SIZE, SIZE / 2>(a, b, lane);
+  if constexpr (SIZE < 64) tile_sort<SIZE * 2>(a, b, lane);
+}
+
+// Sorts s[0, n) descending with tmp[0, n) as scratch; returns the buffer that holds
+// the result.  Every thread of the block (kThreads) must call.
+__device__ unsigned long long *block_sort_desc(unsigned long long *s, unsigned long long *tmp, int n) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPerThread = kSortCap / kThreads;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ntiles = n >> 6;
+  {
+    unsigned long long a[kTilesPerWarp], b[kTilesPerWarp];
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int t = warp + j * kWarps;
+      if (t < ntiles) {
+        a[j] = s[t * 64 + lane];
+        b[j] = s[t * 64 + 32 + lane];
       }
-      const int next = stride > 1 ? (stride >> 1) : size;
-      if (!one_pair || stride >= 32 || next >= 32) __syncthreads();
-      else __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j)
+      if (warp + j * kWarps < ntiles) tile_sort<2>(a[j], b[j], lane);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int t = warp + j * kWarps;
+      if (t < ntiles) {
+        s[t * 64 + lane] = a[j];
+        s[t * 64 + 32 + lane] = b[j];
+      }
     }
   }
   __syncthreads();
+  unsigned long long *src = s, *dst = tmp;
+  for (int lg = 6; (1 << lg) < n; ++lg) {
+    const int m = 1 << lg;
+    unsigned long long x[kPerThread];
+    const unsigned long long *other[kPerThread];
+    bool left[kPerThread];
+    int pos[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      const int i = min(k * kThreads + static_cast<int>(threadIdx.x), n - 1);
+      x[k] = src[i];
+      other[k] = src + (((i >> lg) ^ 1) << lg);
+      left[k] = ((i >> lg) & 1) == 0;
+      pos[k] = 0;
+    }
+    // pos = number of partner keys placed before x (binary lifting over a sorted run)
+    for (int step = m >> 1; step > 0; step >>= 1) {
+#pragma unroll
+      for (int k = 0; k < kPerThread; ++k) {
+        if (k * kThreads >= n) break;   // uniform over the block
+        const unsigned long long v = other[k][pos[k] + step - 1];
+        if (left[k] ? v > x[k] : v >= x[k]) pos[k] += step;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+      if (k * kThreads >= n) break;
+      const unsigned long long v = other[k][pos[k]];
+      if (left[k] ? v > x[k] : v >= x[k]) pos[k] += 1;
+      const int i = k * kThreads + static_cast<int>(threadIdx.x);
+      if (i < n) dst[((i >> (lg + 1)) << (lg + 1)) + (i & (m - 1)) + pos[k]] = x[k];
+    }
+    __syncthreads();
+    unsigned long long *t = src;
+    src = dst;
+    dst = t;
+  }
+  return src;
 }
 
-__device__ __forceinline__ int pow2_at_least(int n) {
-  int p = 1;
+__device__ __forceinline__ int sort_size(int n);
+
+// Sorts s[0, n) descending (1 <= n <= kSortCap) by an order-preserving bucket pass:
+// the keys' top 32 bits (the radix key of the score) relative to their minimum, cut
+// to 12 bits (the span's top 12 significant bits), give 4096 buckets; a counting
+// pass places each bucket's keys in a contiguous group, and each key's rank
+// among the members of its group (all 64 bits compared) gives its final slot.
+// When some group holds more than kGroupMax keys (many equal or near-equal
+// scores) the segment is sorted by block_sort_desc instead.  tmp[] (kSortCap keys)
+// and start[], cur[] (4096 words each) are scratch.  Returns the buffer holding
+// the result.  Every thread of the block must call.
+constexpr int kBuckets = 4096;
+constexpr int kGroupMax = 64;
+
+__device__ unsigned long long *block_bucket_sort_desc(unsigned long long *s, unsigned long long *tmp, int n,
+                                                      uint32_t *start, uint32_t *cur, uint32_t *scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // 1. range of the 32-bit score keys
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t k = static_cast<uint32_t>(s[i] >> 32);
+    lo = min(lo, k);
+    hi = max(hi, k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  for (int i = tid; i < kBuckets; i += kThreads) {
+    start[i] = 0u;
+    cur[i] = 0u;
+  }
+  if (lane == 0) {
+    scratch[warp] = lo;
+    scratch[16 + warp] = hi;
+  }
+  __syncthreads();
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    lo = min(lo, scratch[w]);
+    hi = max(hi, scratch[16 + w]);
+  }
+  const uint32_t span = hi - lo;
+  const int shift = span < static_cast<uint32_t>(kBuckets) ? 0 : 32 - __clz(static_cast<int>(span >> 12));
+  // 2. bucket counts
+  for (int i = tid; i < n; i += kThreads)
+    atomicAdd(&start[(static_cast<uint32_t>(s[i] >> 32) - lo) >> shift], 1u);
+  __syncthreads();
+  // 3. start of each bucket's group, buckets taken from the top; the largest group
+  constexpr int per = kBuckets / kThreads;
+  uint32_t c[per], sum = 0u, big = 0u;
+#pragma unroll
+  for (int m = 0; m < per; ++m) {
+    c[m] = start[kBuckets - 1 - (tid * per + m)];
+    sum += c[m];
+    big = max(big, c[m]);
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan(sum, scratch, &total);
+#pragma unroll
+  for (int m = 0; m < per; ++m) {
+    start[kBuckets - 1 - (tid * per + m)] = run;
+    run += c[m];
+  }
+  const bool fallback = __syncthreads_or(big > static_cast<uint32_t>(kGroupMax)) != 0;
+  if (fallback) {
+    const int p2 = sort_size(n);
+    for (int i = n + tid; i < p2; i += kThreads) s[i] = 0ull;
+    __syncthreads();
+    return block_sort_desc(s, tmp, p2);
+  }
+  // 4. each key into its group (arbitrary order within the group)
+  for (int i = tid; i < n; i += kThreads) {
+    const unsigned long long x = s[i];
+    const uint32_t b = (static_cast<uint32_t>(x >> 32) - lo) >> shift;
+    tmp[start[b] + atomicAdd(&cur[b], 1u)] = x;
+  }
+  __syncthreads();
+  // 5. rank within the group
+  for (int i = tid; i < n; i += kThreads) {
+    const unsigned long long x = tmp[i];
+    const uint32_t b = (static_cast<uint32_t>(x >> 32) - lo) >> shift;
+    const uint32_t g0 = start[b], g1 = start[b] + cur[b];
+    uint32_t r = 0u;
+    for (uint32_t j = g0; j < g1; ++j) r += tmp[j] > x ? 1u : 0u;
+    s[g0 + r] = x;
+  }
+  __syncthreads();
+  return s;
+}
+
+__device__ __forceinline__ int sort_size(int n) {
+  int p = 64;
   while (p < n) p <<= 1;
   return p;
 }
@@ -276,21 +575,25 @@ __device__ __forceinline__ int digit_width(int d) { return d < 2 ? 10 : d < 4 ? 
 
 __device__ __forceinline__ unsigned long long low52(unsigned long long c) { return c & ((1ull << 52) - 1); }
 
-// Threshold on the low 52 bits such that exactly `need` keys of the threshold
-// bin are >= it.  `candidate(i, valid)` yields the i-th key (valid = false to skip).
+// Threshold on the low 52 bits such that exactly `need` of the keys yielded by
+// `candidate(i, valid)` (valid = false to skip) are >= it, by digits d0..4 of
+// the low 52 bits, starting at digit `d0` (the keys agree on the digits above
+// it).  Bits of the returned threshold above digit d0 are 0.
 template <typename Get>
 __device__ unsigned long long select_threshold(int64_t n, uint32_t need, Get candidate, uint32_t *h /* 2048 */,
-                                               uint32_t *scratch) {
+                                               uint32_t *scratch, int d0) {
+  const int top = digit_shift(d0) + digit_width(d0);
   unsigned long long pre = 0ull;
-  for (int d = 0; d < 5; ++d) {
+  for (int d = d0; d < 5; ++d) {
     const int sh = digit_shift(d), wd = digit_width(d);
     const int nb = 1 << wd;
+    const unsigned long long upper = ((1ull << (top - sh - wd)) - 1) << (sh + wd);   // digits d0 .. d-1
     for (int i = threadIdx.x; i < nb; i += blockDim.x) h[i] = 0u;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
       bool valid;
-      const unsigned long long v = low52(candidate(i, valid));
-      if (!valid || (d > 0 && (v >> (sh + wd)) != (pre >> (sh + wd)))) continue;
+      const unsigned long long v = candidate(i, valid);
+      if (!valid || (v & upper) != pre) continue;
       atomicAdd(&h[(v >> sh) & (nb - 1u)], 1u);
     }
     __syncthreads();
@@ -305,107 +608,140 @@ __device__ unsigned long long select_threshold(int64_t n, uint32_t need, Get can
   return pre;
 }
 
+// Appends `take` lanes' keys to list[] at slots counted by *counter (shared).
+__device__ __forceinline__ void warp_push64(bool take, unsigned long long value, unsigned long long *list,
+                                            uint32_t *counter, uint32_t cap) {
+  const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+  if (ballot == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(ballot) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(ballot)));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
+  if (take && at < cap) list[at] = value;
+}
+
 __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   extern __shared__ unsigned long long sm[];
-  __shared__ uint32_t off[kHistBins];
+  unsigned long long *cand = sm;               // [kTieCap]
+  unsigned long long *sel = sm + kTieCap;      // [kSortCap]
+  uint32_t *bstart = reinterpret_cast<uint32_t *>(sel + kSortCap);   // [kBuckets]
+  uint32_t *bcur = bstart + kBuckets;                                // [kBuckets]
+  __shared__ uint32_t hbuf[2048];
   __shared__ uint32_t scratch[36];
-  __shared__ uint32_t bounds_s[2];
   __shared__ uint32_t count_s;
   grid_dependency_wait();   // every collect slice has placed its keys
   const int part = blockIdx.x;
   const int r = blockIdx.y;
+  const int tid = threadIdx.x;
   const Workspace &ws = a.ws;
   const int32_t B = a.bound[r];
   const int K = a.K;
   const int nout = min(K, max(B, 0));
-  uint32_t T, above;
-  row_layout(ws.hist12 + static_cast<int64_t>(r) * kHistBins, B, K, off, scratch, &T, &above);
-  above = min(above, static_cast<uint32_t>(nout));
+  const RowSelect &rs = ws.rowsel[r];
   int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
-  unsigned long long *s = sm;
 
   if (part < kParts) {
-    // This part's winner segment: from the first bin starting at or after
-    // part * S to the first bin starting at or after (part + 1) * S.
-    const uint32_t S = (above + kParts - 1) / kParts;
-    const uint32_t lo_cut = part * S, hi_cut = (part + 1) * S;
-    if (threadIdx.x == 0) {
-      bounds_s[0] = above;
-      bounds_s[1] = above;
-    }
-    __syncthreads();
-    for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) {
-      if (T != kNoBin && static_cast<uint32_t>(b) <= T) continue;
-      const uint32_t o = off[b];
-      if (o >= above) continue;
-      if (o >= lo_cut) atomicMin(&bounds_s[0], o);
-      if (o >= hi_cut) atomicMin(&bounds_s[1], o);
-    }
-    __syncthreads();
-    const uint32_t s0 = bounds_s[0], s1 = max(bounds_s[0], bounds_s[1]);
-    const int n = static_cast<int>(s1 - s0);
-    if (n == 0) return;
+    // the whole winner row is loaded at once (no wait for the cuts first)
     const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
-    const int p2 = pow2_at_least(n);
-    for (int i = threadIdx.x; i < p2; i += blockDim.x) s[i] = i < n ? __ldcg(&win[s0 + i]) : 0ull;
+    unsigned long long w[kSortCap / kThreads];
+#pragma unroll
+    for (int m = 0; m < kSortCap / kThreads; ++m) {
+      const int i = m * kThreads + tid;
+      w[m] = i < K ? __ldcg(&win[i]) : 0ull;
+    }
+    const uint32_t s0 = __ldcg(&rs.cut[part]), s1 = __ldcg(&rs.cut[part + 1]);
+    const int n = static_cast<int>(s1) - static_cast<int>(s0);
+    if (n <= 0) return;
+#pragma unroll
+    for (int m = 0; m < kSortCap / kThreads; ++m) {
+      const int i = m * kThreads + tid - static_cast<int>(s0);
+      if (i >= 0 && i < n) sel[i] = w[m];
+    }
     __syncthreads();
-    bitonic_sort_desc(s, p2);
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-      out[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(s[i] & 0xFFFFFFFFull));
+    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch);
+    for (int i = tid; i < n; i += kThreads)
+      out[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
     return;
   }
 
   // The threshold bin's part: the `need` best candidates after the winners.
+  const uint32_t above = __ldcg(&rs.above);
+  const uint32_t nt = __ldcg(&rs.tie_count);
+  const uint32_t T = __ldcg(&rs.T);
+  const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
+  unsigned long long tv[kTieCap / kThreads];   // the list is read whole, before its length is known
+#pragma unroll
+  for (int m = 0; m < kTieCap / kThreads; ++m) tv[m] = __ldcg(&tie[m * kThreads + tid]);
+  for (int i = tid; i < kSubBins; i += kThreads) hbuf[i] = __ldcg(&ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i]);
+  if (tid == 0) count_s = 0;
   const uint32_t need = static_cast<uint32_t>(nout) - above;
-  for (int j = nout + threadIdx.x; j < K; j += blockDim.x) out[j] = -1;
+  for (int j = nout + tid; j < K; j += kThreads) out[j] = -1;
   if (need == 0) return;
-  const uint32_t nt = __ldcg(&ws.rowsel[r].tie_count);
-  unsigned long long *cand = sm;
-  if (threadIdx.x == 0) count_s = 0;
-  unsigned long long th;
   if (nt <= static_cast<uint32_t>(kTieCap)) {
-    const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
-    for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x) cand[i] = __ldcg(&tie[i]);
+#pragma unroll
+    for (int m = 0; m < kTieCap / kThreads; ++m)
+      if (static_cast<uint32_t>(m * kThreads + tid) < nt) cand[m * kThreads + tid] = tv[m];
     __syncthreads();
-    th = select_threshold(static_cast<int64_t>(nt), need,
-                          [&](int64_t i, bool &valid) { valid = true; return cand[i]; }, off, scratch);
-    // keep the chosen ones at the front (the threshold pass is done with cand)
+    // second digit: the bin S2 holding the need-th candidate
+    uint32_t S2, above2;
+    find_bin(hbuf, kSubBins, need, &S2, &above2, scratch);
+    const uint32_t need2 = need - above2;
+    const uint32_t cnt2 = hbuf[S2];
     __syncthreads();
-    unsigned long long mine[kTieCap / kThreads];
-    int nm = 0;
-    for (uint32_t i = threadIdx.x; i < nt; i += blockDim.x)
-      if (low52(cand[i]) >= th) mine[nm++] = cand[i];
-    __syncthreads();
-    for (int m = 0; m < nm; ++m) cand[atomicAdd(&count_s, 1u)] = mine[m];
-  } else {
-    // Too many keys in the threshold bin for the list: the same digits, over the row.
-    const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-    th = select_threshold(static_cast<int64_t>(B), need,
-                          [&](int64_t pos, bool &valid) {
-                            const uint32_t key = radix_key(row[pos]);
-                            valid = (key >> 20) == T;
-                            return composite(key, pos);
-                          },
-                          off, scratch);
-    __syncthreads();
-    for (int64_t pos = threadIdx.x; pos < B; pos += blockDim.x) {
-      const uint32_t key = radix_key(row[pos]);
-      if ((key >> 20) != T) continue;
-      const unsigned long long c = composite(key, pos);
-      if (low52(c) >= th) {
-        const uint32_t at = atomicAdd(&count_s, 1u);
-        if (at < static_cast<uint32_t>(kSortCap)) cand[at] = c;
+    // the rest of S2's bin, by the 42 bits below the second digit (skipped when the whole bin goes)
+    unsigned long long th42 = 0ull;
+    if (need2 < cnt2)
+      th42 = select_threshold(static_cast<int64_t>(nt), need2,
+                              [&](int64_t i, bool &valid) {
+                                const unsigned long long v = low52(cand[i]);
+                                valid = (v >> 42) == S2;
+                                return v;
+                              },
+                              hbuf, scratch, 1);
+    for (uint32_t i0 = tid & ~31u; i0 < nt; i0 += kThreads) {
+      const uint32_t i = i0 + (tid & 31);
+      bool take = false;
+      unsigned long long c = 0ull;
+      if (i < nt) {
+        c = cand[i];
+        const unsigned long long v = low52(c);
+        const uint32_t sub = static_cast<uint32_t>(v >> 42);
+        take = sub > S2 || (sub == S2 && (v & ((1ull << 42) - 1)) >= th42);
       }
+      warp_push64(take, c, sel, &count_s, static_cast<uint32_t>(kSortCap));
+    }
+  } else {
+    // Too many keys in the threshold bin for the list: digits over the row's scores.
+    __syncthreads();
+    const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
+    const unsigned long long th = select_threshold(
+        static_cast<int64_t>(B), need,
+        [&](int64_t pos, bool &valid) {
+          const uint32_t key = radix_key(row[pos]);
+          valid = (key >> 20) == T;
+          return low52(composite(key, pos));
+        },
+        hbuf, scratch, 0);
+    __syncthreads();
+    for (int64_t p0 = tid & ~31; p0 < B; p0 += kThreads) {
+      const int64_t pos = p0 + (tid & 31);
+      bool take = false;
+      unsigned long long c = 0ull;
+      if (pos < B) {
+        const uint32_t key = radix_key(row[pos]);
+        c = composite(key, pos);
+        take = (key >> 20) == T && low52(c) >= th;
+      }
+      warp_push64(take, c, sel, &count_s, static_cast<uint32_t>(kSortCap));
     }
   }
   __syncthreads();
   const int n = min(static_cast<int>(count_s), static_cast<int>(need));
-  const int p2 = pow2_at_least(n);
-  for (int i = n + threadIdx.x; i < p2; i += blockDim.x) cand[i] = 0ull;
-  __syncthreads();
-  bitonic_sort_desc(cand, p2);
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    out[above + i] = static_cast<int32_t>(~static_cast<uint32_t>(cand[i] & 0xFFFFFFFFull));
+  const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch);
+  for (int i = tid; i < n; i += kThreads)
+    out[above + i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
 }
 
 }  // namespace
@@ -424,30 +760,29 @@ cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream) {
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmem);
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmemAlloc);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCollectSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ns, a.R);
-  cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
+  cfg.gridDim = dim3(ns, a.R);
+  cfg.blockDim = dim3(kCollectThreads);
+  cfg.dynamicSmemBytes = kCollectSmem;
   cudaError_t e = cudaLaunchKernelEx(&cfg, collect_kernel, a);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t fcfg = {};
-  fcfg.gridDim = dim3(kParts + 1, a.R);
-  fcfg.blockDim = dim3(kThreads);
-  fcfg.dynamicSmemBytes = kFinishSmem;
-  fcfg.stream = stream;
-  fcfg.attrs = attr;
-  fcfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&fcfg, finish_kernel, a);
+  cfg.gridDim = dim3(kParts + 1, a.R);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kFinishSmemAlloc;
+  return cudaLaunchKernelEx(&cfg, finish_kernel, a);
 }
 
 }  // namespace idx
