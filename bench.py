@@ -74,7 +74,8 @@ def profile_traffic(kernel_src: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms from before the
+    warm-up to the end; summary() keeps the samples read inside a given window."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -82,22 +83,28 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []   # (host time read, line)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
         return self
 
+    def wait_first(self, timeout_s: float = 5.0):
+        """Blocks until the sampler has printed once (nvidia-smi takes a while to start)."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.01)
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -107,10 +114,12 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0: float, t1: float):
         sm, smax, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for t, line in self.lines:
+            if not (t0 <= t <= t1 + 0.15):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -126,37 +135,51 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(prob, orc, budget_s: float = 20.0):
-    """The oracle (score + exact top-k) on a bounded sample of the workload: whole
-    rows of the first request, as many as fit the time budget (at least one)."""
-    import numpy as np
+def _row_sample(prob, rows, bound):
     import workloads
-    rows = [r for r in range(prob.R) if prob.row_req[r] == 0]
-    # time one row on a slice first to size the sample
-    sub = workloads.Problem(name="sample", q=prob.q[rows[:1]], w=prob.w[rows[:1]], k_cache=prob.k_cache,
-                            k_scale=prob.k_scale, page_table=prob.page_table, row_req=prob.row_req[rows[:1]],
-                            row_bound=prob.row_bound[rows[:1]], kv_dtype=prob.kv_dtype, K=prob.K)
+    return workloads.Problem(name="sample", q=prob.q[rows], w=prob.w[rows], k_cache=prob.k_cache,
+                             k_scale=prob.k_scale, page_table=prob.page_table, row_req=prob.row_req[rows],
+                             row_bound=bound, kv_dtype=prob.kv_dtype, K=prob.K)
+
+
+def _oracle_pass(orc, sub):
+    import numpy as np
     t0 = time.perf_counter()
     s = orc.score(sub)
     orc.topk(s.astype(np.float32), sub.row_bound, sub.K)
-    dt = time.perf_counter() - t0
-    done_rows, done_keys, total_t = 1, int(sub.row_bound.sum()), dt
-    n_more = max(0, min(len(rows) - 1, int((budget_s - dt) / max(dt, 1e-6))))
-    if n_more > 0:
-        sel = rows[1:1 + n_more]
-        sub2 = workloads.Problem(name="sample", q=prob.q[sel], w=prob.w[sel], k_cache=prob.k_cache,
-                                 k_scale=prob.k_scale, page_table=prob.page_table, row_req=prob.row_req[sel],
-                                 row_bound=prob.row_bound[sel], kv_dtype=prob.kv_dtype, K=prob.K)
-        t0 = time.perf_counter()
-        s = orc.score(sub2)
-        orc.topk(s.astype(np.float32), sub2.row_bound, sub2.K)
-        total_t += time.perf_counter() - t0
-        done_rows += n_more
-        done_keys += int(sub2.row_bound.sum())
-    return {"value": done_keys / total_t, "unit": "key·rows/s", "cores": orc.num_threads(),
-            "kind": "oracle", "seconds": round(total_t, 3),
-            "sample": f"{done_rows} of {prob.R} rows of the workload (whole rows, {done_keys} key-rows): "
-                      "oracle scores in fp64 + exact top-2048 by sort"}
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(prob, orc, budget_s: float = 20.0, rate_hint=None):
+    """The oracle (score + exact top-k) on a bounded sample of the workload.
+
+    The sample is rows of the first request in order, the last one cut to the
+    first L keys (a multiple of the 64-key page) so that the pass takes about
+    budget_s; the rate is sized on a 16-page probe of the first row unless a
+    rate from an earlier call is given."""
+    import numpy as np
+    rows = [r for r in range(prob.R) if prob.row_req[r] == 0]
+    rate = rate_hint
+    if rate is None:
+        probe = _row_sample(prob, rows[:1], np.array([min(1024, int(prob.row_bound[rows[0]]))], dtype=np.int32))
+        _oracle_pass(orc, probe)                                   # warm (thread pool, pages)
+        rate = int(probe.row_bound.sum()) / _oracle_pass(orc, probe)
+    want = max(1024, int(rate * budget_s))
+    bounds, take = [], []
+    for r in rows:
+        b = int(prob.row_bound[r])
+        cut = min(b, max(64, (want - sum(bounds)) // 64 * 64))
+        bounds.append(cut)
+        take.append(r)
+        if sum(bounds) >= want or cut < b:
+            break
+    sub = _row_sample(prob, take, np.array(bounds, dtype=np.int32))
+    dt = _oracle_pass(orc, sub)
+    keys = int(sum(bounds))
+    return {"value": keys / dt, "unit": "key·rows/s", "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 3), "rate": keys / dt,
+            "sample": f"{len(take)} of {prob.R} rows of the workload with bounds {bounds} "
+                      f"({keys} key-rows): oracle scores in fp64 + exact top-2048 by sort"}
 
 
 def run_reference(args):
@@ -167,11 +190,13 @@ def run_reference(args):
     import workloads
     orc = oracle.default()
     prob = workloads.make_config(3)
-    vals = []
-    for _ in range(args.warmup):
-        cpu_baseline(prob, orc, budget_s=2.0)
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(prob, orc, budget_s=args.ref_budget))
+    # the whole run (warm-up + timed steps) is held to about --ref-budget seconds
+    per_step = max(0.02, args.ref_budget / max(1, args.steps + args.warmup))
+    first = cpu_baseline(prob, orc, budget_s=per_step)
+    rate = first["rate"]
+    for _ in range(max(0, args.warmup - 1)):
+        cpu_baseline(prob, orc, budget_s=per_step, rate_hint=rate)
+    vals = [cpu_baseline(prob, orc, budget_s=per_step, rate_hint=rate) for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     ms = prob.key_rows / v * 1e3
     line = {
@@ -181,7 +206,7 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "global_batch": prob.R, "seq_len": prob.max_bound,
                    "parallelism": "host cores (oracle)", "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": v, "unit": "key·rows/s", "cores": vals[0]["cores"], "kind": "oracle",
-                         "sample": vals[0]["sample"]},
+                         "sample": "per step: " + vals[0]["sample"]},
         "e2e": {"value": v, "unit": "key·rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -191,13 +216,14 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="3", help="workload: 0..4 or 3a (default 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="seconds for the whole --impl reference run")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not os.environ.get("IDX_BENCH_ALLOW_SHORT"):
         print("note: warm-up raised to 3 steps", file=sys.stderr)
@@ -241,6 +267,8 @@ def main():
         if ev is not None:
             ev[1].record(stream)
 
+    clocks = ClockSampler(local).__enter__()
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -262,12 +290,14 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            step(evs[i], sevs[i])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        step(evs[i], sevs[i])
+    torch.cuda.synchronize()
+    t_end = time.perf_counter()
+    t_wall = t_end - t_start
+    time.sleep(0.15)   # the sample that covers the end of the timed region
+    clocks.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
     st = dp.status()
@@ -363,7 +393,7 @@ def main():
                          "launch_frac_of_roofline": t_roof / (ms * 1e-3),
                          "tensor_frac_fp8": flops / score_s / 1e12 / fp8_tf,
                          "tensor_frac_bf16_precision_matched": flops / score_s / 1e12 / bf16_tf},
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(t_start, t_end),
             "gpu_launches": KERNELS_PER_LAUNCH * args.steps,
             "wall_s_timed_region": t_wall,
         }
