@@ -213,6 +213,36 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------- multi-rank host logic
+def rank_problem(cfg, rank: int):
+    """The workload of one rank: rank 0 runs the named configuration itself, rank
+    r > 0 the same shapes drawn with seed offset 1000 * r, so every rank holds an
+    independent batch (the path shards by request, with no exchange)."""
+    import workloads
+    return workloads.make_config(cfg, seed_offset=1000 * rank)
+
+
+def max_over_ranks(values, device: str):
+    """Elementwise maximum of per-rank timings over the process group (every rank
+    gets the result)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def total_key_rows(key_rows_per_rank: int, world: int) -> int:
+    """Whole-job units: every rank scores a batch of the same shape."""
+    return int(key_rows_per_rank) * int(world)
+
+
+def emit(line, rank: int):
+    """Rank 0 prints the JSON line; the other ranks print nothing."""
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -246,12 +276,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     cfg = args.config if args.config == "3a" else int(args.config)
-    if world > 1 and rank > 0 and cfg == 3:
-        # each rank its own batch of two 512K-key requests
-        prob = workloads.build(workloads.CONFIG_NAMES[3], [524288, 524288], [4, 4], "e4m3",
-                               seed=3 + 1000 * rank, key_dist="mixture")
-    else:
-        prob = workloads.make_config(cfg)
+    prob = rank_problem(cfg, rank)
     dp = lib.DeviceProblem(prob)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
@@ -342,11 +367,10 @@ def main():
 
     # max over ranks
     if world > 1:
-        t = torch.tensor([ms, score_mean_ms, e2e_ms or 0.0], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, score_mean_ms, e2e_ms = float(t[0]), float(t[1]), (float(t[2]) or None)
+        ms, score_mean_ms, e2e_ms = max_over_ranks([ms, score_mean_ms, e2e_ms or 0.0], "cuda")
+        e2e_ms = e2e_ms or None
 
-    key_rows_total = prob.key_rows * world
+    key_rows_total = total_key_rows(prob.key_rows, world)
     value = key_rows_total / (ms * 1e-3)
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
     fp8_tf = 2.0 * bf16_tf     # FP8 dense = 2 x bf16 dense (nominal ratio)
@@ -403,7 +427,7 @@ def main():
         if not args.no_cpu_baseline:
             import oracle
             line["cpu_baseline"] = cpu_baseline(prob, oracle.default())
-        print(json.dumps(line))
+    emit(line if rank == 0 else None, rank)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -230,31 +230,36 @@ CONFIG_NAMES = {
 }
 
 
-def make_config(cfg) -> Problem:
-    """The named workloads (see CONFIG_NAMES)."""
+def make_config(cfg, seed_offset: int = 0) -> Problem:
+    """The named workloads (see CONFIG_NAMES).  A nonzero seed_offset draws the same
+    shapes (lengths, rows, bounds) with other values and page permutations."""
+    return _make_config(cfg, seed_offset)
+
+
+def _make_config(cfg, off: int) -> Problem:
     if cfg == 0:
-        return build(CONFIG_NAMES[0], [4096], [1], "e4m3", seed=0,
+        return build(CONFIG_NAMES[0], [4096], [1], "e4m3", seed=0 + off,
                      bounds=[[4096]], recipe="q N(0,1) bf16; w N(0,1)/8; keys N(0,1) -> E4M3, scale amax/448")
     if cfg == 1:
         L = 131072
-        return build(CONFIG_NAMES[1], [L], [4], "e4m3", seed=1, dup_frac=0.01,
+        return build(CONFIG_NAMES[1], [L], [4], "e4m3", seed=1 + off, dup_frac=0.01,
                      recipe="as cfg0; bounds L-3..L; 1% of positions exact copies of others")
     if cfg == 2:
         rng = np.random.default_rng(1002)
         lengths = _log_uniform(rng, 8, 8192, 262144)
-        return build(CONFIG_NAMES[2], lengths, [4] * 8, "e4m3", seed=2,
+        return build(CONFIG_NAMES[2], lengths, [4] * 8, "e4m3", seed=2 + off,
                      recipe=f"lengths {lengths}; bounds L-3..L; one globally shuffled page pool")
     if cfg == 3:
-        return build(CONFIG_NAMES[3], [524288, 524288], [4, 4], "e4m3", seed=3, key_dist="mixture",
+        return build(CONFIG_NAMES[3], [524288, 524288], [4, 4], "e4m3", seed=3 + off, key_dist="mixture",
                      recipe="keys sigma in {1,4} w.p. 1/2 per token -> E4M3; bounds L-3..L")
     if cfg == "3a":
-        return build(CONFIG_NAMES["3a"], [524288], [4], "e4m3", seed=3, key_dist="mixture",
+        return build(CONFIG_NAMES["3a"], [524288], [4], "e4m3", seed=3 + off, key_dist="mixture",
                      recipe="first request of cfg3 alone")
     if cfg == 4:
         rng = np.random.default_rng(1004)
         rows = [int(x) for x in rng.integers(1, 5, size=64)]
         lengths = _log_uniform(rng, 64, 1024, 524288)
-        return build(CONFIG_NAMES[4], lengths, rows, "bf16", seed=4,
+        return build(CONFIG_NAMES[4], lengths, rows, "bf16", seed=4 + off,
                      recipe="bf16 keys N(0,1); rows U{1..4}; lengths log-uniform 1K-512K")
     raise ValueError(cfg)
 
