@@ -158,6 +158,33 @@ int64_t idx_debug_set(int32_t what, int64_t value);
  * cudaEventElapsedTime.  Applies to one call, then clears itself.  Process-wide. */
 void idx_profile_events(void *start, void *stop);
 
+/* Exact top-K of given scores with no caller workspace.  The page has no
+ * counterpart: this is idx_topk run on scratch that lives in the library itself,
+ * a file-scope device array of IDX_NOALLOC_SCRATCH_BYTES (enough for up to
+ * IDX_NOALLOC_MAX_ROWS rows at any K up to IDX_MAX_K and any max_bound).  It is
+ * for callers that cannot allocate device memory on their decode path: a host
+ * program that links only this library and has no device allocator of its own,
+ * or a serving loop that reserves all its memory up front because an allocation
+ * between steps can synchronise the device or fail under memory pressure.  The
+ * call allocates nothing.
+ *   scores, ld, row_bound, R, max_bound, K, out_idx: as for idx_topk (no hist).
+ *   R > IDX_NOALLOC_MAX_ROWS returns IDX_EUNSUPPORTED and launches nothing; the
+ *   other argument checks are those of idx_topk (IDX_EINVAL).
+ *   Setup: the first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress) and keeps it for later calls; make that first call on
+ *   each device before any stream capture begins.  A failed lookup returns
+ *   IDX_ECUDA.
+ *   Nothing in the scratch has to start at zero: every call clears the selection
+ *   state it uses before its kernels read it.
+ *   The scratch is one per device and process: two calls whose work can overlap
+ *   in time (different streams, or different host threads) race on it, and the
+ *   caller must order them (e.g. one stream).  Device-detected errors (a row bound
+ *   outside [0, max_bound], clamped as idx_topk does) have no readback here. */
+#define IDX_NOALLOC_MAX_ROWS 8
+#define IDX_NOALLOC_SCRATCH_BYTES (1280 * 1024)
+idx_status idx_topk_noalloc(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R,
+                            int32_t max_bound, int32_t K, int32_t *out_idx, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

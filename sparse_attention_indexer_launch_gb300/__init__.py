@@ -24,7 +24,7 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
-           "idx_debug_set", "idx_profile_events"]
+           "idx_debug_set", "idx_profile_events", "idx_topk_noalloc"]
 
 
 class IdxError(RuntimeError):
@@ -73,6 +73,8 @@ def _load():
     lib.idx_debug_set.restype = i64
     lib.idx_profile_events.argtypes = [vp, vp]
     lib.idx_profile_events.restype = None
+    lib.idx_topk_noalloc.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp]
+    lib.idx_topk_noalloc.restype = ctypes.c_int
     return lib
 
 
@@ -129,6 +131,11 @@ def idx_topk(scores, ld: int, row_bound, R: int, max_bound: int, K: int, hist, o
     _check(lib.idx_topk(_ptr(scores), int(ld), _ptr(row_bound), int(R), int(max_bound), int(K),
                         _ptr(hist), _ptr(out_idx), _ptr(ws), ws.numel() * ws.element_size(),
                         _stream(stream)), "idx_topk")
+
+
+def idx_topk_noalloc(scores, ld: int, row_bound, R: int, max_bound: int, K: int, out_idx, stream=None):
+    _check(lib.idx_topk_noalloc(_ptr(scores), int(ld), _ptr(row_bound), int(R), int(max_bound), int(K),
+                                _ptr(out_idx), _stream(stream)), "idx_topk_noalloc")
 
 
 def idx_launch(problem: Problem, K: int, out_idx, ws, stream=None):

@@ -206,6 +206,16 @@ idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, 
   return IDX_OK;
 }
 
+
+// Scratch of idx_topk_noalloc: a file-scope device array, so that the call takes
+// no workspace from the caller and allocates nothing.  Its address is looked up
+// once per device; the workspace starts at the first 1024-byte boundary inside
+// it (the loaded module guarantees a smaller alignment only), so up to
+// IDX_NOALLOC_SCRATCH_BYTES - 1023 bytes are usable.
+__device__ __align__(256) unsigned char g_noalloc_scratch[IDX_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void *g_noalloc_base[128] = {};
+
 }  // namespace
 
 extern "C" {
@@ -403,6 +413,31 @@ int64_t idx_debug_set(int32_t what, int64_t value) {
     g_stall_next = value > 0 ? value : 0;
   }
   return prev;
+}
+
+idx_status idx_topk_noalloc(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R,
+                            int32_t max_bound, int32_t K, int32_t *out_idx, void *stream) {
+  if (R > IDX_NOALLOC_MAX_ROWS) return IDX_EUNSUPPORTED;
+  if (R < 1 || K < 1 || K > IDX_MAX_K || max_bound < 0) return IDX_EINVAL;
+  const Layout L = make_layout(R, K, max_bound, false);
+  if (L.total > IDX_NOALLOC_SCRATCH_BYTES - (kAlign - 1)) return IDX_EUNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ECUDA;
+  if (dev < 0 || dev >= 128) return IDX_EUNSUPPORTED;
+  void *base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_base[dev] == nullptr) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return IDX_ECUDA;
+      g_noalloc_base[dev] = p;
+    }
+    base = g_noalloc_base[dev];
+  }
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(base);
+  const uintptr_t aligned = (raw + kAlign - 1) & ~static_cast<uintptr_t>(kAlign - 1);
+  return idx_topk(scores, ld, row_bound, R, max_bound, K, nullptr, out_idx, reinterpret_cast<void *>(aligned),
+                  IDX_NOALLOC_SCRATCH_BYTES - (aligned - raw), stream);
 }
 
 }  // extern "C"
