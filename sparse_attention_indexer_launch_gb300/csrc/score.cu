@@ -22,9 +22,11 @@
 //               (bulk copy) on group changes;
 //   warp 1      MMA issuer (one thread) and TMEM owner; two accumulators in TMEM,
 //               so the MMA of tile k+1 runs while tile k's epilogue reads;
-//   warps 2..17 epilogue, four sets of four (one warp per TMEM lane quarter);
-//               set i reduces row i of the group for every tile, so each warp
-//               keeps one row's weights and one row's histogram.
+//   warps 2..17 epilogue, two groups of eight taking alternate tiles (group g
+//               reads accumulator g), four warps per TMEM lane quarter; each warp
+//               reduces two rows of its group's tiles for its quarter, so the
+//               per-tile costs (waits, scales, hand-back) are paid once per two
+//               rows and the groups work out of step with each other.
 // E4M3 cache: keys feed tcgen05.mma kind::f8f6f4 straight from the TMA ring; the
 // query is split exactly into two E4M3 terms (prep.cu), run as K = 2 x 128.
 // bf16 cache: keys and query are bf16, kind::f16, K = 128.
@@ -59,8 +61,8 @@ struct Barriers {
   uint64_t bfull;
   uint64_t bfree;
   uint64_t drain;
-  uint64_t hdone[4];     // per epilogue set: its four warps finished adding to the histogram
-  uint64_t hflushed[4];  // per epilogue set: its four warps finished flushing it
+  uint64_t hdone[1];     // every epilogue warp finished adding to the histograms
+  uint64_t hflushed[1];  // every epilogue warp finished flushing them
   uint32_t tmem_base;
   int abort;
 };
@@ -72,7 +74,7 @@ struct Smem {
   static constexpr int kHist = kA + Cfg<KV>::kStages * Cfg<KV>::kStageBytes;
   static constexpr int kScales = kHist + kMaxGroupRows * kHistWords * 4;
   static constexpr int kW = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
-  static constexpr int kBars = kW + kEpiWarps * kHeads * 4;
+  static constexpr int kBars = kW + kEpiWarps * 2 * kHeads * 4;
   static constexpr int kBytes = kBars + static_cast<int>(sizeof(Barriers));
   static constexpr int kDynamic = kBytes + 1024;  // alignment slack
 };
@@ -183,16 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     for (int s = 0; s < kScaleSlots; ++s) {
       mbar_init(&bars->sfull[s], 32);          // one cp.async arrival per producer lane
-      mbar_init(&bars->sempty[s], kEpiWarps);
+      mbar_init(&bars->sempty[s], kEpiWarps / 2);   // the eight warps of the tile's group
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->tfull[s], 1);
-      mbar_init(&bars->tempty[s], kEpiWarps);
+      mbar_init(&bars->tempty[s], kEpiWarps / 2);
     }
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(&bars->hdone[s], 4);
-      mbar_init(&bars->hflushed[s], 4);
-    }
+    mbar_init(&bars->hdone[0], kEpiWarps);
+    mbar_init(&bars->hflushed[0], kEpiWarps);
     mbar_init(&bars->bfull, 1);
     mbar_init(&bars->bfree, 1);
     mbar_init(&bars->drain, 1);
@@ -376,81 +376,103 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    // Two groups of eight warps take alternate tiles (group g reads accumulator g);
+    // within a group each warp reduces two rows of the tile for its TMEM lane quarter.
     const int ew = warp - 2;
-    const int set = ew >> 2;                 // the group row this warp reduces
     const int quarter = warp & 3;            // TMEM lane quarter this warp may read
-    const int wq4 = ew & 3;                  // this warp's share of the row's histogram flush
-    float *myw = sw + ew * kHeads;
-    uint32_t *h = shist + set * kHistWords;
+    const int slot = ew >> 2;                // 0..3 among the quarter's four warps
+    const int tg = slot & 1;                 // tile parity this warp handles
+    const int r0 = (slot >> 1) * 2;          // first of this warp's two group rows
+    float *myw = sw + ew * 2 * kHeads;       // the two rows' weights
     GroupCursor cur;
     cur.seek(ws.groups, num_groups, static_cast<int>(t0));
     int cur_g = -1;
     Group grp;
     grp.nrows = 0;
     grp.row0 = 0;
-    bool mine = false;
-    int32_t bnd = 0;
+    bool mine[2] = {false, false};
+    int32_t bnd[2] = {0, 0};
     int flushes = 0;
-    int tiles_since_flush = 0;
     bool ok = true;
 
-    // The set's histogram row goes to global memory (12-bit counts and, when asked,
-    // the 64-bin first digit) and is cleared; the set's four warps meet before and after.
+    // Every row's histogram goes to global memory (12-bit counts and, when asked,
+    // the 64-bin first digit) and is cleared; all sixteen warps meet before and
+    // after, each flushing 16 of the 4 x 64 (row, first digit) blocks.
     auto flush = [&]() -> bool {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->hdone[set]);
-      if (!mbar_wait(&bars->hdone[set], flushes & 1, limit, abort)) return false;
-      if (mine) {
-        const int64_t grow = grp.row0 + set;
-        for (int d = wq4 * 16; d < wq4 * 16 + 16; ++d) {   // 16 first digits per warp
-          const uint32_t wv = h[d * 32 + lane];
-          const uint32_t lo = wv & 0xFFFFu, hi = wv >> 16;
-          if (wv) {
-            h[d * 32 + lane] = 0u;
-            if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
-            if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
-          }
-          if (a.hist != nullptr) {
-            const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
-            if (lane == 0 && dsum) atomicAdd(&a.hist[grow * 64 + d], dsum);
-          }
+      if (lane == 0) mbar_arrive(&bars->hdone[0]);
+      if (!mbar_wait(&bars->hdone[0], flushes & 1, limit, abort)) return false;
+      for (int b = ew * 16; b < ew * 16 + 16; ++b) {
+        const int row = b >> 6, d = b & 63;
+        if (row >= grp.nrows) break;       // uniform for the warp
+        uint32_t *h = shist + row * kHistWords;
+        const int64_t grow = grp.row0 + row;
+        const uint32_t wv = h[d * 32 + lane];
+        const uint32_t lo = wv & 0xFFFFu, hi = wv >> 16;
+        if (wv) {
+          h[d * 32 + lane] = 0u;
+          if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
+          if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
+        }
+        if (a.hist != nullptr) {
+          const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
+          if (lane == 0 && dsum) atomicAdd(&a.hist[grow * 64 + d], dsum);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->hflushed[set]);
-      const bool r = mbar_wait(&bars->hflushed[set], flushes & 1, limit, abort);
+      if (lane == 0) mbar_arrive(&bars->hflushed[0]);
+      const bool r = mbar_wait(&bars->hflushed[0], flushes & 1, limit, abort);
       ++flushes;
-      tiles_since_flush = 0;
       return r;
     };
 
-    for (int64_t t = t0; t < t1; ++t) {
-      const int k = static_cast<int>(t - t0);
-      if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
-        if (cur_g >= 0 && !flush()) {
-          ok = false;
-          break;
-        }
-        cur_g = cur.g;
-        grp = ws.groups[cur_g];
-        mine = set < grp.nrows;
-        bnd = mine ? ws.bound_eff[grp.row0 + set] : 0;
-        __syncwarp();
-        if (mine) {
-          const float2 v = reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(grp.row0 + set) * kHeads)[lane];
-          reinterpret_cast<float2 *>(myw)[lane] = v;
-        }
-        __syncwarp();
-      } else if (tiles_since_flush >= kFlushTiles) {
-        if (!flush()) {
-          ok = false;
-          break;
+    // The two groups see different tiles, so the flush points (every group start
+    // and every kFlushTiles tiles within a group; 16-bit counters) are defined on
+    // the CTA's tile sequence and every warp takes each of them, in order.
+    auto load_group = [&]() {
+      grp = ws.groups[cur.g];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mine[i] = r0 + i < grp.nrows;
+        bnd[i] = mine[i] ? ws.bound_eff[grp.row0 + r0 + i] : 0;
+        if (mine[i]) {
+          const float2 v =
+              reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(grp.row0 + r0 + i) * kHeads)[lane];
+          reinterpret_cast<float2 *>(myw + i * kHeads)[lane] = v;
         }
       }
-      ++tiles_since_flush;
+      __syncwarp();
+    };
+    int64_t done = t0;   // flush points at or before this tile are taken
+    auto catch_up = [&](int64_t upto) -> bool {   // takes every flush point p in (done, upto]
+      for (;;) {
+        const int64_t periodic =
+            grp.tile_begin + ((done - grp.tile_begin) / kFlushTiles + 1) * static_cast<int64_t>(kFlushTiles);
+        const int64_t p = periodic < cur.next_begin ? periodic : static_cast<int64_t>(cur.next_begin);
+        if (p > upto) break;
+        if (!flush()) return false;
+        if (p == cur.next_begin) {
+          cur.advance(static_cast<int>(p));
+          load_group();
+        }
+        done = p;
+      }
+      if (upto > done) done = upto;
+      return true;
+    };
+    load_group();
+    cur_g = cur.g;
+
+    for (int64_t t = t0 + tg; t < t1; t += 2) {
+      const int k = static_cast<int>(t - t0);
+      if (!catch_up(t)) {
+        ok = false;
+        break;
+      }
       const int j = static_cast<int>(t) - grp.tile_begin;
       const int64_t pos = static_cast<int64_t>(j) * kTileKeys + quarter * 32 + lane;
-      const int acc = k & 1;
+      const int acc = tg;
       const int ss = k % kScaleSlots;
       float scale = 1.0f;
       if (KV == IDX_KV_E4M3) {
@@ -469,13 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         break;
       }
       tc_fence_after();
-      float score = 0.f;
+      float score[2] = {0.f, 0.f};
       const bool valid = pos < grp.L;
-      if (mine) {
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256 + set * 64;
-        const bool neg = valid && scale < 0.0f;
-        const bool any_neg = __any_sync(0xffffffffu, neg);
-        const float4 *w4 = reinterpret_cast<const float4 *>(myw);
+      const bool neg = valid && scale < 0.0f;
+      const bool any_neg = __any_sync(0xffffffffu, neg);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (!mine[i]) continue;            // uniform for the warp
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256 + (r0 + i) * 64;
+        const float4 *w4 = reinterpret_cast<const float4 *>(myw + i * kHeads);
         float2 accs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -486,20 +510,23 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           if (!any_neg) relu_dot32(v, w4 + half * 8, accs);
           else relu_dot32_signed(v, w4 + half * 8, neg, accs);
         }
-        score = (((accs[0].x + accs[0].y) + (accs[1].x + accs[1].y)) + ((accs[2].x + accs[2].y) + (accs[3].x + accs[3].y))) * scale;
+        score[i] = (((accs[0].x + accs[0].y) + (accs[1].x + accs[1].y)) + ((accs[2].x + accs[2].y) + (accs[3].x + accs[3].y))) * scale;
       }
       // Accumulator read: hand it back to the MMA issuer.
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tempty[acc]);
-      if (mine) {
-        const bool keep = valid && pos < bnd;
-        if (keep) a.scores[static_cast<int64_t>(grp.row0 + set) * a.ld + pos] = score;
-        const uint32_t bin = radix_key(score) >> (32 - kHistBits);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (!mine[i]) continue;
+        const bool keep = valid && pos < bnd[i];
+        if (keep) a.scores[static_cast<int64_t>(grp.row0 + r0 + i) * a.ld + pos] = score[i];
+        const uint32_t bin = radix_key(score[i]) >> (32 - kHistBits);
+        uint32_t *h = shist + (r0 + i) * kHistWords;
         if (keep) atomicAdd(&h[bin >> 1], 1u << ((bin & 1) * 16));   // shared-memory atomics resolve collisions
       }
     }
-    if (ok && cur_g >= 0) flush();
+    if (ok && catch_up(t1 - 1)) flush();
   }
 
   // Every role is done (or gave up); release TMEM.
