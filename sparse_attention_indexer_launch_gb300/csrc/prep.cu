@@ -223,6 +223,9 @@ __device__ void clear_row_state(const PrepArgs &a, int r) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+  // The scoring launch may start its CTAs now: they set up shared memory, barriers
+  // and TMEM, then wait for this grid to finish before reading anything it writes.
+  grid_dependency_trigger();
   if (blockIdx.x == a.R) {
     plan_block(a);
   } else {

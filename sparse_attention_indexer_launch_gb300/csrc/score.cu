@@ -170,14 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   const int lane = threadIdx.x & 31;
   const Workspace &ws = a.ws;
 
-  grid_dependency_wait();   // the plan and the query operands come from the prep launch
-  const int total_tiles = ws.plan->total_tiles;
-  const int num_groups = ws.plan->num_groups;
-  const int64_t t0 = static_cast<int64_t>(total_tiles) * blockIdx.x / gridDim.x;
-  const int64_t t1 = static_cast<int64_t>(total_tiles) * (blockIdx.x + 1) / gridDim.x;
-  grid_dependency_trigger();
-  if (t0 >= t1) return;  // uniform for the CTA: nothing allocated yet
-
+  // Set-up that reads nothing from the prep launch runs before waiting for it.
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -208,6 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_wait();   // the plan and the query operands come from the prep launch
+  const int total_tiles = ws.plan->total_tiles;
+  const int num_groups = ws.plan->num_groups;
+  const int64_t t0 = static_cast<int64_t>(total_tiles) * blockIdx.x / gridDim.x;
+  const int64_t t1 = static_cast<int64_t>(total_tiles) * (blockIdx.x + 1) / gridDim.x;
+  grid_dependency_trigger();
+  if (t0 >= t1) {  // uniform for the CTA: no tiles, give the TMEM back
+    if (warp == 1) tmem_dealloc(bars->tmem_base, kTmemCols);
+    return;
+  }
   const uint32_t tmem_base = bars->tmem_base;
   const uint64_t limit = a.wait_limit_ns;
   volatile int *abort = &bars->abort;
