@@ -31,7 +31,7 @@ uint64_t wait_limit() {
 }
 
 struct Layout {
-  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, cursor, hist_sub, rowsel, win, tie, scores;
+  size_t status, plan, groups, bound_eff, qop0, qop1, wq, hist12, hist64, hist_sub, rowsel, win, tie, scores;
   size_t total;
   int64_t scores_ld;
 };
@@ -52,7 +52,7 @@ Layout make_layout(int64_t R, int64_t K, int64_t max_bound, bool with_scores) {
   L.qop1 = take(static_cast<size_t>(R) * idx::kRowOperandBytes);
   L.wq = take(static_cast<size_t>(R) * idx::kHeads * 4);
   L.hist12 = take(static_cast<size_t>(R) * idx::kHistBins * 4);
-  L.cursor = take(static_cast<size_t>(R) * idx::kHistBins * 4);
+  L.hist64 = take(static_cast<size_t>(R) * 64 * 4);
   L.hist_sub = take(static_cast<size_t>(R) * idx::kSubBins * 4);
   L.rowsel = take(static_cast<size_t>(R) * sizeof(idx::RowSelect));
   L.win = take(static_cast<size_t>(R) * K * 8);
@@ -74,7 +74,7 @@ Workspace carve(void *base, const Layout &L) {
   w.qop1 = b + L.qop1;
   w.wq = reinterpret_cast<float *>(b + L.wq);
   w.hist12 = reinterpret_cast<uint32_t *>(b + L.hist12);
-  w.cursor = reinterpret_cast<uint32_t *>(b + L.cursor);
+  w.hist64 = reinterpret_cast<uint32_t *>(b + L.hist64);
   w.hist_sub = reinterpret_cast<uint32_t *>(b + L.hist_sub);
   w.rowsel = reinterpret_cast<idx::RowSelect *>(b + L.rowsel);
   w.win = reinterpret_cast<unsigned long long *>(b + L.win);
@@ -261,6 +261,7 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
   a.ws = w;
   a.bulk_rows = (reinterpret_cast<uintptr_t>(scores) & 15u) == 0 && ld % 4 == 0;
   a.wait_limit_ns = wait_limit();
+  a.num_sms = sms;
   st = cuda_ok(idx::launch_select_clear(a, row_bound, s));
   if (st != IDX_OK) return st;
   st = cuda_ok(idx::launch_hist12(a, s));
@@ -290,6 +291,10 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   a.ws = w;
   a.bulk_rows = (reinterpret_cast<uintptr_t>(w.scores) & 15u) == 0 && w.scores_ld % 4 == 0;
   a.wait_limit_ns = wait_limit();
+  int sms = 0;
+  st = device_sms(&sms);
+  if (st != IDX_OK) return st;
+  a.num_sms = sms;
   return cuda_ok(idx::launch_collect(a, s));
 }
 

@@ -44,9 +44,8 @@ struct PlanHeader {
 struct RowSelect {       // per-row selection state
   uint32_t tie_count;    // keys in the threshold bin, appended by the collect kernel
   uint32_t T;            // 12-bit bin holding the k-th key (0xFFFFFFFF: the row keeps all keys)
-  uint32_t above;        // keys in higher bins (= the winners)
-  uint32_t pad;
-  uint32_t cut[8];       // winner slots cut into bin-aligned segments, one per finish part
+  uint32_t win_count;    // keys in higher bins (the winners), appended by the collect kernel
+  uint32_t pad[5];
 };
 
 // The fused score histogram counts the top kHistBits bits of radix_key(score):
@@ -64,10 +63,10 @@ struct Workspace {
   uint8_t *qop1;           // [R][8192]  FP8: q_lo; bf16: dims 64..127
   float *wq;               // [R][64]    weights / 2 with the query prescale folded in
   uint32_t *hist12;        // [R][4096]  12-bit histogram of the radix keys
-  uint32_t *cursor;        // [R][4096]  keys placed so far per 12-bit bin
+  uint32_t *hist64;        // [R][64]    its 64-bin marginal (the first digit radix_key >> 26)
   uint32_t *hist_sub;      // [R][1024]  second-digit histogram of the threshold bin
   RowSelect *rowsel;       // [R]
-  unsigned long long *win; // [R][K]     keys above the threshold bin, grouped by bin (composite keys)
+  unsigned long long *win; // [R][K]     keys above the threshold bin, in arrival order (composite keys)
   unsigned long long *tie; // [R][kTieCap] keys in the threshold bin
   float *scores;           // [R][ld]    score scratch of idx_launch (else unused)
   int64_t scores_ld;

@@ -41,6 +41,8 @@ struct SelectArgs {
   Workspace ws;
   int32_t bulk_rows;       // scores and ld allow 16-byte bulk copies of row slices
   uint64_t wait_limit_ns;
+  int32_t num_sms;         // SMs of the device (sizes the collect grid)
+  int32_t slice;           // keys per collect CTA (set by launch_collect)
 };
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);

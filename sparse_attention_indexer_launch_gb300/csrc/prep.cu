@@ -214,8 +214,8 @@ __device__ void clear_row_state(const PrepArgs &a, int r) {
   if (a.hist_target != nullptr && threadIdx.x < 64) a.hist_target[r * 64 + threadIdx.x] = 0u;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
     ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
-    if (a.clear_select) ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
   }
+  if (threadIdx.x < 64) ws.hist64[static_cast<int64_t>(r) * 64 + threadIdx.x] = 0u;
   if (a.clear_select)
     for (int i = threadIdx.x; i < kSubBins; i += blockDim.x) ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i] = 0u;
   if (a.clear_select && threadIdx.x < sizeof(RowSelect) / 4)

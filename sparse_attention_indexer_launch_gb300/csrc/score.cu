@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     int flushes = 0;
     bool ok = true;
 
-    // Every row's histogram goes to global memory (12-bit counts and, when asked,
-    // the 64-bin first digit) and is cleared; all sixteen warps meet before and
+    // Every row's histogram goes to global memory (12-bit counts, the 64-bin first
+    // digit, and the caller's copy of the latter when asked) and is cleared; all sixteen warps meet before and
     // after, each flushing 16 of the 4 x 64 (row, first digit) blocks.
     auto flush = [&]() -> bool {
       __syncwarp();
@@ -417,9 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
           if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
         }
-        if (a.hist != nullptr) {
-          const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
-          if (lane == 0 && dsum) atomicAdd(&a.hist[grow * 64 + d], dsum);
+        const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
+        if (lane == 0 && dsum) {
+          atomicAdd(&ws.hist64[grow * 64 + d], dsum);
+          if (a.hist != nullptr) atomicAdd(&a.hist[grow * 64 + d], dsum);
         }
       }
       __syncwarp();

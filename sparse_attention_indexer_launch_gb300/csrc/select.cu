@@ -16,33 +16,37 @@
 // the number of keys in higher bins: its exclusive prefix from the top.  The bin
 // T holding the k-th key is where that prefix crosses K, and every key in a
 // higher bin b belongs at output slots [prefix(b), prefix(b) + count(b)).
-//   collect  one CTA per slice of kSlice keys of a row: the slice is copied to
-//            shared memory while the CTA scans the row's histogram for T and the
-//            prefixes.  Keys above T are listed, then written straight into
-//            their bin's slots (a per-bin cursor orders keys within the bin
-//            arbitrarily); keys in T are appended to the row's candidate list and
-//            counted in a 1024-bin histogram of their next 10 bits (the second
-//            digit).  The first slice also records T and the cuts of the winner
-//            slots into kParts bin-aligned segments.
-//   finish   kParts CTAs per row sort the winners' segments in place (bins are
-//            contiguous ranges of slots, so segments sort independently); one
-//            more CTA per row takes the candidates whose second digit is above
-//            the one holding the k-th key, picks the rest from that digit's bin by
-//            the remaining 42 bits, sorts them into the slots after the winners
-//            and writes -1 past min(K, bound).  A row with more candidates than
-//            the list holds (thousands of equal scores) is resolved digit by
-//            digit over the row's scores instead.
+//   collect  one CTA per slice of a row (up to kSlice keys, sized so that the grid
+//            is about four CTAs per SM): the slice is copied to
+//            shared memory while one warp finds T from the row's 64-bin first
+//            digit and the 64 twelve-bit bins of that digit.  Keys above T (the
+//            winners) are appended to the row's winner list; keys in T (the
+//            candidates) to its candidate list, and counted in a 1024-bin
+//            histogram of their next 10 bits (the second digit).
+//   finish   kParts CTAs per row each scan the row's 12-bit histogram for the
+//            first output slot of every bin above T, cut the winner slots into
+//            kParts bin-aligned segments and sort the winners of their segment
+//            into it.  One more CTA per row takes the candidates whose second
+//            digit is above the one holding the k-th key, picks the rest from
+//            that digit's bin by the remaining 42 bits, sorts them into the slots
+//            after the winners and writes -1 past min(K, bound).  A row with more
+//            candidates than the list holds (thousands of equal scores) is
+//            resolved digit by digit over the row's scores instead.
 #include "idx_device.cuh"
 #include "launch.h"
 
 namespace idx {
 namespace {
 
-constexpr int kSlice = 8192;
+constexpr int kSlice = 8192;              // largest slice (the page's limit)
+constexpr int kSliceStep = 1024;          // slices are multiples of this (4 keys x 256 threads)
 constexpr int kCollectThreads = 256;
 constexpr int kWinList = IDX_MAX_K;        // winners of one slice (at most K)
 constexpr int kCandList = 4096;            // candidates of one slice kept in shared memory
-constexpr int kCollectSmem = kSlice * 4 + (kWinList + kCandList) * 2 + kHistBins * 2;
+constexpr int kCollectSmem = kSlice * 4 + (kWinList + kCandList) * 2;
+// Requested per collect CTA: more than a fifth of an SM's shared memory, so that
+// at most four CTAs share an SM and the grid spreads over all SMs.
+constexpr int kCollectSmemAlloc = 52 * 1024;
 constexpr int kThreads = 512;              // hist12 and finish
 constexpr int kParts = 4;                  // winner segments per row
 constexpr int kSortCap = IDX_MAX_K;        // power of two
@@ -53,9 +57,8 @@ constexpr int kFinishSmem = (kTieCap + kSortCap) * 8 + 2 * 4096 * 4;   // candid
 constexpr int kFinishSmemAlloc = 120 * 1024;
 static_assert(kFinishSmem <= kFinishSmemAlloc, "finish shared memory");
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
-static_assert(kParts + 1 <= 8, "RowSelect holds the cuts");
 static_assert(kTilesPerWarp >= 1 && kSortCap % 64 == 0, "sort tiles");
-static_assert(kCollectSmem <= 54 * 1024, "four collect CTAs per SM");
+static_assert(kCollectSmem <= kCollectSmemAlloc, "collect shared memory");
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t pos) {
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
@@ -131,11 +134,9 @@ __device__ void find_bin(const uint32_t *hist, int nbins, uint32_t need, uint32_
 __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound) {
   const int r = blockIdx.x;
   const Workspace &ws = a.ws;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
-    ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
-    ws.cursor[static_cast<int64_t>(r) * kHistBins + i] = 0u;
-  }
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) ws.hist12[static_cast<int64_t>(r) * kHistBins + i] = 0u;
   for (int i = threadIdx.x; i < kSubBins; i += blockDim.x) ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i] = 0u;
+  if (threadIdx.x < 64) ws.hist64[static_cast<int64_t>(r) * 64 + threadIdx.x] = 0u;
   if (threadIdx.x < sizeof(RowSelect) / 4) reinterpret_cast<uint32_t *>(&ws.rowsel[r])[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     const int32_t b = row_bound[r];
@@ -145,7 +146,8 @@ __global__ void select_clear_kernel(const SelectArgs a, const int32_t *row_bound
   }
 }
 
-// The 12-bit histogram of given scores (one slice of a row per CTA).
+// The 12-bit histogram of given scores and its 64-bin marginal (one slice of a
+// row per CTA).
 __global__ void __launch_bounds__(kThreads) hist12_kernel(const SelectArgs a) {
   __shared__ uint32_t h[kHistBins];
   const int r = blockIdx.y;
@@ -160,6 +162,45 @@ __global__ void __launch_bounds__(kThreads) hist12_kernel(const SelectArgs a) {
   __syncthreads();
   for (int i = threadIdx.x; i < kHistBins; i += kThreads)
     if (h[i]) atomicAdd(&a.ws.hist12[static_cast<int64_t>(r) * kHistBins + i], h[i]);
+  // marginal: warp w sums first digits w, w + 16, ...
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int d = warp; d < 64; d += kThreads / 32) {
+    const uint32_t c = __reduce_add_sync(0xffffffffu, h[d * 64 + lane] + h[d * 64 + 32 + lane]);
+    if (lane == 0 && c) atomicAdd(&a.ws.hist64[static_cast<int64_t>(r) * 64 + d], c);
+  }
+}
+
+// The bin holding the need-th key of 64 counts taken from the top, by one warp:
+// lane l holds count[63 - l] and count[31 - l].  Returns the bin (or kNoBin when
+// the counts sum below need) and the keys in higher bins.
+__device__ __forceinline__ uint32_t warp_find64(uint32_t c_hi, uint32_t c_lo, uint32_t need, uint32_t *above) {
+  const int lane = threadIdx.x & 31;
+  uint32_t inc_hi = c_hi, inc_lo = c_lo;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t a = __shfl_up_sync(0xffffffffu, inc_hi, o);
+    const uint32_t b = __shfl_up_sync(0xffffffffu, inc_lo, o);
+    if (lane >= o) {
+      inc_hi += a;
+      inc_lo += b;
+    }
+  }
+  const uint32_t tot_hi = __shfl_sync(0xffffffffu, inc_hi, 31);
+  inc_lo += tot_hi;
+  const uint32_t m_hi = __ballot_sync(0xffffffffu, inc_hi >= need);
+  const uint32_t m_lo = __ballot_sync(0xffffffffu, inc_lo >= need);
+  if (m_hi) {
+    const int l = __ffs(m_hi) - 1;
+    *above = __shfl_sync(0xffffffffu, inc_hi - c_hi, l);
+    return 63u - l;
+  }
+  if (m_lo) {
+    const int l = __ffs(m_lo) - 1;
+    *above = __shfl_sync(0xffffffffu, inc_lo - c_lo, l);
+    return 31u - l;
+  }
+  *above = __shfl_sync(0xffffffffu, inc_lo, 31);
+  return kNoBin;
 }
 
 // ---------------------------------------------------------------------------- collect
@@ -182,10 +223,8 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   float *vals = reinterpret_cast<float *>(csm);                               // [kSlice]
   uint16_t *wlist = reinterpret_cast<uint16_t *>(csm + kSlice * 4);           // [kWinList]
   uint16_t *clist = wlist + kWinList;                                         // [kCandList]
-  uint16_t *off = clist + kCandList;                                          // [kHistBins], winner bins only
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t scratch[36];
-  __shared__ uint32_t cuts[kParts + 1];
   __shared__ uint32_t nwin, ncand;
   __shared__ int abort_flag;
 
@@ -194,10 +233,11 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
   const int32_t B = a.bound[r];
-  if (static_cast<int>(blockIdx.x) >= nslices(B)) return;
+  const int slice = a.slice;
+  if (static_cast<int>(blockIdx.x) >= (B > 0 ? (B + slice - 1) / slice : 1)) return;
   const Workspace &ws = a.ws;
-  const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(B), begin + kSlice) - begin));
+  const int64_t begin = static_cast<int64_t>(blockIdx.x) * slice;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(B), begin + slice) - begin));
   const float *src = a.scores + static_cast<int64_t>(r) * a.ld + begin;
 
   // 1. the slice into shared memory (one bulk copy when the rows are 16-byte aligned)
@@ -216,72 +256,30 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   if (!a.bulk_rows)
     for (int i = tid; i < n; i += kCollectThreads) vals[i] = __ldcg(src + i);
 
-  // 2. meanwhile: the row's 12-bit layout (T, keys above T, the winner bins' slots).
-  //    The histogram is staged through shared memory (over the lists, which are not
-  //    in use yet) by coalesced loads; each thread then scans a run of `per` bins.
-  constexpr int per = kHistBins / kCollectThreads;
-  static_assert(per % 4 == 0 && kHistBins * 4 <= (kWinList + kCandList) * 2 + kHistBins * 2, "histogram staging");
-  uint32_t *hs = reinterpret_cast<uint32_t *>(wlist);
-  const uint4 *hg = reinterpret_cast<const uint4 *>(ws.hist12 + static_cast<int64_t>(r) * kHistBins);
-  for (int i = tid; i < kHistBins / 4; i += kCollectThreads) reinterpret_cast<uint4 *>(hs)[i] = __ldcg(&hg[i]);
-  __syncthreads();
-  uint32_t c[per];   // this thread's bins, highest first: bins 4095 - tid * per - m
-  uint32_t sum = 0;
-#pragma unroll
-  for (int k = 0; k < per / 4; ++k) {
-    const uint4 h4 = reinterpret_cast<const uint4 *>(hs + kHistBins - per * (tid + 1))[per / 4 - 1 - k];
-    c[4 * k] = h4.w;
-    c[4 * k + 1] = h4.z;
-    c[4 * k + 2] = h4.y;
-    c[4 * k + 3] = h4.x;
-  }
-#pragma unroll
-  for (int m = 0; m < per; ++m) sum += c[m];
-  uint32_t total;
-  uint32_t run = block_excl_scan(sum, scratch, &total);   // its barriers also end the reads of hs
-  if (tid == 0) {
-    scratch[34] = kNoBin;
-    scratch[35] = static_cast<uint32_t>(max(B, 0));
-  }
-  __syncthreads();
-#pragma unroll
-  for (int m = 0; m < per; ++m) {
-    const int b = kHistBins - 1 - (tid * per + m);
-    off[b] = static_cast<uint16_t>(min(run, 0xFFFFu));
-    if (B > a.K && run < static_cast<uint32_t>(a.K) && static_cast<uint32_t>(a.K) <= run + c[m]) {
-      scratch[34] = static_cast<uint32_t>(b);
-      scratch[35] = run;
+  // 2. meanwhile: the bin T holding the K-th key, from the row's 64-bin first
+  //    digit and that digit's 64 twelve-bit bins (one warp, two dependent loads).
+  if (threadIdx.x < 32) {
+    uint32_t T = kNoBin;
+    if (B > a.K) {
+      const uint32_t *h64 = ws.hist64 + static_cast<int64_t>(r) * 64;
+      uint32_t above_d;
+      const uint32_t D = warp_find64(__ldcg(&h64[63 - tid]), __ldcg(&h64[31 - tid]), static_cast<uint32_t>(a.K),
+                                     &above_d);
+      if (D != kNoBin) {
+        const uint32_t *h12 = ws.hist12 + static_cast<int64_t>(r) * kHistBins + D * 64;
+        uint32_t above_f;
+        const uint32_t f = warp_find64(__ldcg(&h12[63 - tid]), __ldcg(&h12[31 - tid]),
+                                       static_cast<uint32_t>(a.K) - above_d, &above_f);
+        if (f != kNoBin) T = D * 64 + f;
+      }
     }
-    run += c[m];
+    if (tid == 0) {
+      scratch[34] = T;
+      if (blockIdx.x == 0) ws.rowsel[r].T = T;
+    }
   }
   __syncthreads();
   const uint32_t T = scratch[34];
-  const uint32_t above = min(scratch[35], static_cast<uint32_t>(min(a.K, max(B, 0))));
-
-  if (blockIdx.x == 0) {   // the finish kernel's segment cuts: first winner-bin start at or after p * S
-    const uint32_t S = (above + kParts - 1) / kParts;
-    if (tid <= kParts) cuts[tid] = above;
-    __syncthreads();
-    for (int b = tid; b < kHistBins; b += kCollectThreads) {
-      if (T != kNoBin && static_cast<uint32_t>(b) <= T) continue;
-      const uint32_t o = off[b];
-      if (o >= above) continue;
-      for (int p = 1; p < kParts; ++p)
-        if (o >= p * S) atomicMin(&cuts[p], o);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      RowSelect &rs = ws.rowsel[r];
-      rs.T = T;
-      rs.above = above;
-      uint32_t prev = 0u;
-      rs.cut[0] = 0u;
-      for (int p = 1; p <= kParts; ++p) {
-        prev = max(cuts[p], prev);
-        rs.cut[p] = prev;
-      }
-    }
-  }
 
   // 3. classify the slice
   if (a.bulk_rows) {
@@ -298,7 +296,7 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
     const int Tc = static_cast<int>(T);
     const float4 *v4 = reinterpret_cast<const float4 *>(vals);
 #pragma unroll 2
-    for (int i = 0; i < kSlice / 4 / kCollectThreads; ++i) {
+    for (int i = 0; i < slice / 4 / kCollectThreads; ++i) {
       const int q = i * kCollectThreads + tid;
       const float4 x = v4[q];
       const float xs[4] = {x.x, x.y, x.z, x.w};
@@ -321,19 +319,23 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   }
   __syncthreads();
 
-  // 4. winners into their slots; candidates onto the row's list
+  // 4. winners onto the row's winner list; candidates onto its candidate list
   const uint32_t nw = min(nwin, static_cast<uint32_t>(kWinList));
+  const int lane = tid & 31;
+  RowSelect &rs = ws.rowsel[r];
   unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
-  uint32_t *cursor = ws.cursor + static_cast<int64_t>(r) * kHistBins;
-  for (uint32_t i = tid; i < nw; i += kCollectThreads) {
-    const int j = wlist[i];
-    const uint32_t key = radix_key(vals[j]);
-    const uint32_t bin = key >> 20;
-    const uint32_t slot = static_cast<uint32_t>(off[bin]) + atomicAdd(&cursor[bin], 1u);
-    if (slot < static_cast<uint32_t>(a.K)) win[slot] = composite(key, begin + j);
+  for (uint32_t i0 = tid & ~31u; i0 < nw; i0 += kCollectThreads) {   // one warp per 32 winners
+    const uint32_t i = i0 + lane;
+    const uint32_t cnt = min(32u, nw - i0);
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&rs.win_count, cnt);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (i < nw && base + lane < static_cast<uint32_t>(a.K)) {
+      const int j = wlist[i];
+      win[base + lane] = composite(radix_key(vals[j]), begin + j);
+    }
   }
   const uint32_t nc = ncand;
-  RowSelect &rs = ws.rowsel[r];
   if (nc > static_cast<uint32_t>(kCandList)) {
     // more candidates than one slice keeps: the finish resolves the row from its scores
     if (tid == 0) atomicAdd(&rs.tie_count, static_cast<uint32_t>(kTieCap) + 1u);
@@ -341,7 +343,6 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   }
   unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
   uint32_t *hsub = ws.hist_sub + static_cast<int64_t>(r) * kSubBins;
-  const int lane = tid & 31;
   for (uint32_t i0 = tid & ~31u; i0 < nc; i0 += kCollectThreads) {   // one warp per 32 candidates
     const uint32_t i = i0 + lane;
     const uint32_t cnt = min(32u, nc - i0);
@@ -643,31 +644,79 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
 
   if (part < kParts) {
-    // the whole winner row is loaded at once (no wait for the cuts first)
+    // Winner segment `part`: the row's 12-bit histogram gives every bin above T
+    // its first output slot; the winner slots are cut into kParts bin-aligned
+    // segments (cut p is the first bin start at or after p * ceil(winners / kParts))
+    // and this CTA sorts the winners whose bin starts inside its segment.
+    uint32_t *hs = reinterpret_cast<uint32_t *>(cand);                 // [4096] counts, then first slots
+    __shared__ uint32_t cuts_s[kParts + 1];
+    const uint32_t T = __ldcg(&rs.T);
+    const uint32_t nw = min(__ldcg(&rs.win_count), static_cast<uint32_t>(K));
     const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
-    unsigned long long w[kSortCap / kThreads];
+    unsigned long long w[kSortCap / kThreads];   // the whole winner list, loaded before it is needed
 #pragma unroll
     for (int m = 0; m < kSortCap / kThreads; ++m) {
-      const int i = m * kThreads + tid;
-      w[m] = i < K ? __ldcg(&win[i]) : 0ull;
+      const uint32_t i = m * kThreads + tid;
+      w[m] = i < nw ? __ldcg(&win[i]) : 0ull;
     }
-    const uint32_t s0 = __ldcg(&rs.cut[part]), s1 = __ldcg(&rs.cut[part + 1]);
-    const int n = static_cast<int>(s1) - static_cast<int>(s0);
-    if (n <= 0) return;
+    const uint32_t S = (nw + kParts - 1) / kParts;
+    if (tid <= kParts) cuts_s[tid] = nw;
+    const uint4 *hg = reinterpret_cast<const uint4 *>(ws.hist12 + static_cast<int64_t>(r) * kHistBins);
+    for (int i = tid; i < kHistBins / 4; i += kThreads) reinterpret_cast<uint4 *>(hs)[i] = __ldcg(&hg[i]);
+    __syncthreads();
+    constexpr int per = kHistBins / kThreads;    // this thread's bins, highest first
+    uint32_t c[per], sum = 0u;
 #pragma unroll
-    for (int m = 0; m < kSortCap / kThreads; ++m) {
-      const int i = m * kThreads + tid - static_cast<int>(s0);
-      if (i >= 0 && i < n) sel[i] = w[m];
+    for (int m = 0; m < per; ++m) {
+      c[m] = hs[kHistBins - 1 - (tid * per + m)];
+      sum += c[m];
+    }
+    uint32_t total;
+    uint32_t run = block_excl_scan(sum, scratch, &total);   // its barriers end the reads of the counts
+#pragma unroll
+    for (int m = 0; m < per; ++m) {
+      const int b = kHistBins - 1 - (tid * per + m);
+      hs[b] = run;
+      if ((T == kNoBin || static_cast<uint32_t>(b) > T) && run < nw && c[m] > 0u)
+        for (int q = 1; q < kParts; ++q)
+          if (run >= q * S) atomicMin(&cuts_s[q], run);
+      run += c[m];
     }
     __syncthreads();
-    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch);
+    uint32_t s0 = 0u, s1 = nw;
+    {
+      uint32_t prev = 0u;
+      for (int q = 1; q <= part + 1; ++q) {
+        const uint32_t cq = q <= kParts - 1 ? max(cuts_s[q], prev) : nw;
+        if (q == part) s0 = cq;
+        if (q == part + 1) s1 = cq;
+        prev = cq;
+      }
+      if (part == 0) s0 = 0u;
+    }
+    if (s1 <= s0) return;   // uniform: an empty segment
+    if (tid == 0) count_s = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < kSortCap / kThreads; ++m) {
+      const uint32_t i = m * kThreads + tid;
+      bool take = false;
+      if (i < nw) {
+        const uint32_t o = hs[static_cast<uint32_t>(w[m] >> 52)];
+        take = o >= s0 && o < s1;
+      }
+      warp_push64(take, w[m], sel, &count_s, static_cast<uint32_t>(kSortCap));
+    }
+    __syncthreads();
+    const int n = min(static_cast<int>(count_s), static_cast<int>(s1 - s0));
+    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand + kHistBins / 2, n, bstart, bcur, scratch);
     for (int i = tid; i < n; i += kThreads)
       out[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
     return;
   }
 
   // The threshold bin's part: the `need` best candidates after the winners.
-  const uint32_t above = __ldcg(&rs.above);
+  const uint32_t above = min(__ldcg(&rs.win_count), static_cast<uint32_t>(nout));
   const uint32_t nt = __ldcg(&rs.tie_count);
   const uint32_t T = __ldcg(&rs.T);
   const unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
@@ -684,11 +733,43 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
     for (int m = 0; m < kTieCap / kThreads; ++m)
       if (static_cast<uint32_t>(m * kThreads + tid) < nt) cand[m * kThreads + tid] = tv[m];
     __syncthreads();
-    // second digit: the bin S2 holding the need-th candidate
-    uint32_t S2, above2;
-    find_bin(hbuf, kSubBins, need, &S2, &above2, scratch);
-    const uint32_t need2 = need - above2;
+    // Second digit.  The candidates' 1024-bin histogram, summed from the top,
+    // gives each bin's first slot among the candidates; S2 is the bin holding
+    // the need-th.  Every bin above S2 is taken whole, S2 in part.
+    __shared__ uint32_t gmax_s;
+    if (tid == 0) {
+      gmax_s = 0u;
+      scratch[34] = 0u;
+      scratch[35] = 0u;
+    }
+    const int b0 = kSubBins - 1 - 2 * tid, b1 = b0 - 1;   // this thread's two bins, highest first
+    const uint32_t c0 = tid < kSubBins / 2 ? hbuf[b0] : 0u;
+    const uint32_t c1 = tid < kSubBins / 2 ? hbuf[b1] : 0u;
+    uint32_t total;
+    const uint32_t e0 = block_excl_scan(c0 + c1, scratch, &total);
+    const uint32_t e1 = e0 + c0;
+    if (tid < kSubBins / 2) {
+      bstart[b0] = e0;
+      bstart[b1] = e1;
+      bcur[b0] = 0u;
+      bcur[b1] = 0u;
+      if (e0 < need && need <= e1) {
+        scratch[34] = static_cast<uint32_t>(b0);
+        scratch[35] = e0;
+      } else if (e1 < need && need <= e1 + c1) {
+        scratch[34] = static_cast<uint32_t>(b1);
+        scratch[35] = e1;
+      }
+      // the largest group of equal 22-bit prefixes among the keys taken
+      const uint32_t g0 = e0 < need ? min(c0, need - e0) : 0u;
+      const uint32_t g1 = e1 < need ? min(c1, need - e1) : 0u;
+      if (max(g0, g1) > 0u) atomicMax(&gmax_s, max(g0, g1));
+    }
+    __syncthreads();
+    const uint32_t S2 = scratch[34];
+    const uint32_t need2 = need - scratch[35];
     const uint32_t cnt2 = hbuf[S2];
+    const uint32_t gmax = gmax_s;
     __syncthreads();
     // the rest of S2's bin, by the 42 bits below the second digit (skipped when the whole bin goes)
     unsigned long long th42 = 0ull;
@@ -700,18 +781,30 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
                                 return v;
                               },
                               hbuf, scratch, 1);
-    for (uint32_t i0 = tid & ~31u; i0 < nt; i0 += kThreads) {
-      const uint32_t i = i0 + (tid & 31);
-      bool take = false;
-      unsigned long long c = 0ull;
-      if (i < nt) {
-        c = cand[i];
-        const unsigned long long v = low52(c);
-        const uint32_t sub = static_cast<uint32_t>(v >> 42);
-        take = sub > S2 || (sub == S2 && (v & ((1ull << 42) - 1)) >= th42);
+    // each taken key into its second-digit bin's slots (any order within the bin)
+    for (uint32_t i = tid; i < nt; i += kThreads) {
+      const unsigned long long c = cand[i];
+      const unsigned long long v = low52(c);
+      const uint32_t sub = static_cast<uint32_t>(v >> 42);
+      if (sub > S2 || (sub == S2 && (v & ((1ull << 42) - 1)) >= th42)) {
+        const uint32_t slot = bstart[sub] + atomicAdd(&bcur[sub], 1u);
+        if (slot < need) sel[slot] = c;
       }
-      warp_push64(take, c, sel, &count_s, static_cast<uint32_t>(kSortCap));
     }
+    __syncthreads();
+    if (gmax <= static_cast<uint32_t>(kGroupMax)) {
+      // order within each bin by the rank among its members (all 64 bits compared)
+      for (uint32_t i = tid; i < need; i += kThreads) {
+        const unsigned long long x = sel[i];
+        const uint32_t sub = static_cast<uint32_t>(low52(x) >> 42);
+        const uint32_t g0 = bstart[sub], g1 = g0 + bcur[sub];
+        uint32_t rank = 0u;
+        for (uint32_t j = g0; j < g1; ++j) rank += sel[j] > x ? 1u : 0u;
+        out[above + g0 + rank] = static_cast<int32_t>(~static_cast<uint32_t>(x & 0xFFFFFFFFull));
+      }
+      return;
+    }
+    if (tid == 0) count_s = need;   // many equal prefixes: sort the taken keys below
   } else {
     // Too many keys in the threshold bin for the list: digits over the row's scores.
     __syncthreads();
@@ -757,15 +850,29 @@ cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream) {
+// Slice length for the collect grid: about four CTAs per SM over all rows,
+// a multiple of kSliceStep, at most kSlice.
+int collect_slice(const SelectArgs &a) {
+  const int64_t keys = static_cast<int64_t>(a.R) * (a.max_bound > 1 ? a.max_bound : 1);
+  const int64_t ctas = 4LL * (a.num_sms > 1 ? a.num_sms : 1);
+  int64_t s = (keys + ctas - 1) / ctas;
+  s = (s + kSliceStep - 1) / kSliceStep * kSliceStep;
+  if (s < kSliceStep) s = kSliceStep;
+  if (s > kSlice) s = kSlice;
+  return static_cast<int>(s);
+}
+
+cudaError_t launch_collect(const SelectArgs &a_in, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmemAlloc);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCollectSmem);
+    e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCollectSmemAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  SelectArgs a = a_in;
+  a.slice = collect_slice(a);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -773,10 +880,10 @@ cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int ns = max(1, (a.max_bound + kSlice - 1) / kSlice);
+  const int ns = max(1, (a.max_bound + a.slice - 1) / a.slice);
   cfg.gridDim = dim3(ns, a.R);
   cfg.blockDim = dim3(kCollectThreads);
-  cfg.dynamicSmemBytes = kCollectSmem;
+  cfg.dynamicSmemBytes = kCollectSmemAlloc;
   cudaError_t e = cudaLaunchKernelEx(&cfg, collect_kernel, a);
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(kParts + 1, a.R);
