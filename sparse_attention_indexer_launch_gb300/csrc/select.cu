@@ -23,13 +23,12 @@
 //            winners) are appended to the row's winner list; keys in T (the
 //            candidates) to its candidate list, and counted in a 1024-bin
 //            histogram of their next 10 bits (the second digit).
-//   finish   kParts CTAs per row each scan the row's 12-bit histogram for the
-//            first output slot of every bin above T, cut the winner slots into
-//            kParts bin-aligned segments and sort the winners of their segment
-//            into it.  One more CTA per row takes the candidates whose second
-//            digit is above the one holding the k-th key, picks the rest from
-//            that digit's bin by the remaining 42 bits, sorts them into the slots
-//            after the winners and writes -1 past min(K, bound).  A row with more
+//   finish   two CTAs per row.  One sorts the winner list into the first output
+//            slots (the winners are fewer than K).  The other takes the
+//            candidates whose second digit is above the one holding the k-th
+//            key, picks the rest from that digit's bin by the remaining 42 bits,
+//            places them by second digit after the winners, orders each digit's
+//            few keys by rank, and writes -1 past min(K, bound).  A row with more
 //            candidates than the list holds (thousands of equal scores) is
 //            resolved digit by digit over the row's scores instead.
 #include "idx_device.cuh"
@@ -48,7 +47,6 @@ constexpr int kCollectSmem = kSlice * 4 + (kWinList + kCandList) * 2;
 // at most four CTAs share an SM and the grid spreads over all SMs.
 constexpr int kCollectSmemAlloc = 52 * 1024;
 constexpr int kThreads = 512;              // hist12 and finish
-constexpr int kParts = 4;                  // winner segments per row
 constexpr int kSortCap = IDX_MAX_K;        // power of two
 constexpr int kTilesPerWarp = kSortCap / 64 / (kThreads / 32);   // 64-key sort tiles per warp
 constexpr int kFinishSmem = (kTieCap + kSortCap) * 8 + 2 * 4096 * 4;   // candidates, the keys to sort, buckets
@@ -204,20 +202,6 @@ __device__ __forceinline__ uint32_t warp_find64(uint32_t c_hi, uint32_t c_lo, ui
 }
 
 // ---------------------------------------------------------------------------- collect
-// Appends `take` lanes' values to list[] at slots counted by *counter (shared).
-__device__ __forceinline__ void warp_push(bool take, uint16_t value, uint16_t *list, uint32_t *counter,
-                                          uint32_t cap) {
-  const uint32_t ballot = __ballot_sync(0xffffffffu, take);
-  if (ballot == 0u) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(ballot) - 1;
-  uint32_t base = 0;
-  if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(ballot)));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
-  if (take && at < cap) list[at] = value;
-}
-
 __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectArgs a) {
   extern __shared__ __align__(128) unsigned char csm[];
   float *vals = reinterpret_cast<float *>(csm);                               // [kSlice]
@@ -291,70 +275,106 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
     __syncthreads();
   }
   {
-    // winners: bin > Tw; candidates: bin == Tc (Tw = Tc = -1 when the row keeps every key)
-    const int Tw = T == kNoBin ? -1 : static_cast<int>(T);
-    const int Tc = static_cast<int>(T);
+    // The bins become float thresholds (radix_key is monotone, and -0.0 and +0.0
+    // compare equal as floats as they share a key): a winner is x >= fw (its bin
+    // above T), a candidate fc <= x < fw (its bin T).  NaN thresholds take nothing.
+    const float kNegInf = __uint_as_float(0xFF800000u);
+    auto key_floor = [&](uint32_t k) {   // the smallest non-NaN float whose radix key is >= k
+      if (k < 0x00800000u) return kNegInf;   // keys below that of -max are -inf's and NaNs'
+      return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
+    };
+    const float kNaN = __uint_as_float(0x7FC00000u);
+    const float fw = T == kNoBin ? kNegInf
+                                 : (T + 1u < static_cast<uint32_t>(kHistBins) ? key_floor((T + 1u) << 20) : kNaN);
+    const float fc = T == kNoBin ? kNaN : key_floor(T << 20);
     const float4 *v4 = reinterpret_cast<const float4 *>(vals);
-#pragma unroll 2
-    for (int i = 0; i < slice / 4 / kCollectThreads; ++i) {
+    const int nq = slice / 4 / kCollectThreads;   // this thread's key quads, at most 8
+    auto masks = [&](int i, uint32_t &wm, uint32_t &cm) {
       const int q = i * kCollectThreads + tid;
       const float4 x = v4[q];
       const float xs[4] = {x.x, x.y, x.z, x.w};
-      uint32_t wm = 0u, cm = 0u;
+      wm = 0u;
+      cm = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int bin = static_cast<int>(radix_key(xs[e]) >> 20);
         const bool in = 4 * q + e < n;
-        wm |= static_cast<uint32_t>(in && bin > Tw) << e;
-        cm |= static_cast<uint32_t>(in && bin == Tc) << e;
+        const bool w = xs[e] >= fw;
+        wm |= static_cast<uint32_t>(in && w) << e;
+        cm |= static_cast<uint32_t>(in && !w && xs[e] >= fc) << e;
       }
-      if (__any_sync(0xffffffffu, (wm | cm) != 0u)) {   // rare: most keys fall below T
+    };
+    // pass 1: count this thread's winners and candidates, remember the quads holding any
+    uint32_t qmask = 0u, cw = 0u, cc = 0u;
+    for (int i = 0; i < nq; ++i) {
+      uint32_t wm, cm;
+      masks(i, wm, cm);
+      if (wm | cm) {
+        qmask |= 1u << i;
+        cw += __popc(wm);
+        cc += __popc(cm);
+      }
+    }
+    // offsets in the slice's two lists (16-bit fields: at most kSlice keys of each)
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan((cw << 16) | cc, scratch, &tot);
+    uint32_t wpos = ex >> 16, cpos = ex & 0xFFFFu;
+    if (tid == 0) {
+      nwin = tot >> 16;
+      ncand = tot & 0xFFFFu;
+    }
+    // pass 2: the marked quads again, writing the keys' offsets within the slice
+    while (qmask) {
+      const int i = __ffs(qmask) - 1;
+      qmask &= qmask - 1u;
+      uint32_t wm, cm;
+      masks(i, wm, cm);
+      const int j0 = 4 * (i * kCollectThreads + tid);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          warp_push((wm >> e) & 1u, static_cast<uint16_t>(4 * q + e), wlist, &nwin, kWinList);
-          warp_push((cm >> e) & 1u, static_cast<uint16_t>(4 * q + e), clist, &ncand, kCandList);
+      for (int e = 0; e < 4; ++e) {
+        if ((wm >> e) & 1u) {
+          if (wpos < static_cast<uint32_t>(kWinList)) wlist[wpos] = static_cast<uint16_t>(j0 + e);
+          ++wpos;
+        }
+        if ((cm >> e) & 1u) {
+          if (cpos < static_cast<uint32_t>(kCandList)) clist[cpos] = static_cast<uint16_t>(j0 + e);
+          ++cpos;
         }
       }
     }
   }
   __syncthreads();
 
-  // 4. winners onto the row's winner list; candidates onto its candidate list
+  // 4. winners onto the row's winner list; candidates onto its candidate list.
+  //    One thread reserves both ranges (two atomics in flight together).
   const uint32_t nw = min(nwin, static_cast<uint32_t>(kWinList));
-  const int lane = tid & 31;
+  const uint32_t nc = ncand;
   RowSelect &rs = ws.rowsel[r];
+  __shared__ uint32_t wbase_s, cbase_s;
+  if (tid == 0) {
+    wbase_s = nw > 0u ? atomicAdd(&rs.win_count, nw) : 0u;
+    // more candidates than one slice keeps: the finish resolves the row from its scores
+    cbase_s = nc > 0u ? atomicAdd(&rs.tie_count, nc <= static_cast<uint32_t>(kCandList)
+                                                     ? nc : static_cast<uint32_t>(kTieCap) + 1u)
+                      : 0u;
+  }
+  __syncthreads();
   unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
-  for (uint32_t i0 = tid & ~31u; i0 < nw; i0 += kCollectThreads) {   // one warp per 32 winners
-    const uint32_t i = i0 + lane;
-    const uint32_t cnt = min(32u, nw - i0);
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&rs.win_count, cnt);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (i < nw && base + lane < static_cast<uint32_t>(a.K)) {
+  for (uint32_t i = tid; i < nw; i += kCollectThreads) {
+    const uint32_t slot = wbase_s + i;
+    if (slot < static_cast<uint32_t>(a.K)) {
       const int j = wlist[i];
-      win[base + lane] = composite(radix_key(vals[j]), begin + j);
+      win[slot] = composite(radix_key(vals[j]), begin + j);
     }
   }
-  const uint32_t nc = ncand;
-  if (nc > static_cast<uint32_t>(kCandList)) {
-    // more candidates than one slice keeps: the finish resolves the row from its scores
-    if (tid == 0) atomicAdd(&rs.tie_count, static_cast<uint32_t>(kTieCap) + 1u);
-    return;
-  }
+  if (nc > static_cast<uint32_t>(kCandList)) return;
   unsigned long long *tie = ws.tie + static_cast<int64_t>(r) * kTieCap;
   uint32_t *hsub = ws.hist_sub + static_cast<int64_t>(r) * kSubBins;
-  for (uint32_t i0 = tid & ~31u; i0 < nc; i0 += kCollectThreads) {   // one warp per 32 candidates
-    const uint32_t i = i0 + lane;
-    const uint32_t cnt = min(32u, nc - i0);
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&rs.tie_count, cnt);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (i < nc) {
-      const int j = clist[i];
-      const uint32_t key = radix_key(vals[j]);
-      atomicAdd(&hsub[(key >> 10) & (kSubBins - 1)], 1u);
-      if (base + lane < static_cast<uint32_t>(kTieCap)) tie[base + lane] = composite(key, begin + j);
-    }
+  for (uint32_t i = tid; i < nc; i += kCollectThreads) {
+    const int j = clist[i];
+    const uint32_t key = radix_key(vals[j]);
+    atomicAdd(&hsub[(key >> 10) & (kSubBins - 1)], 1u);
+    const uint32_t slot = cbase_s + i;
+    if (slot < static_cast<uint32_t>(kTieCap)) tie[slot] = composite(key, begin + j);
   }
 }
 
@@ -643,75 +663,17 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   const RowSelect &rs = ws.rowsel[r];
   int32_t *out = a.out_idx + static_cast<int64_t>(r) * K;
 
-  if (part < kParts) {
-    // Winner segment `part`: the row's 12-bit histogram gives every bin above T
-    // its first output slot; the winner slots are cut into kParts bin-aligned
-    // segments (cut p is the first bin start at or after p * ceil(winners / kParts))
-    // and this CTA sorts the winners whose bin starts inside its segment.
-    uint32_t *hs = reinterpret_cast<uint32_t *>(cand);                 // [4096] counts, then first slots
-    __shared__ uint32_t cuts_s[kParts + 1];
-    const uint32_t T = __ldcg(&rs.T);
-    const uint32_t nw = min(__ldcg(&rs.win_count), static_cast<uint32_t>(K));
+  if (part == 0) {
+    // The winners (keys above T, fewer than K) are the first output slots: one
+    // bucket sort of the row's whole winner list.
+    const uint32_t nw = min(__ldcg(&rs.win_count), static_cast<uint32_t>(nout));
+    if (nw == 0u) return;
     const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
-    unsigned long long w[kSortCap / kThreads];   // the whole winner list, loaded before it is needed
-#pragma unroll
-    for (int m = 0; m < kSortCap / kThreads; ++m) {
-      const uint32_t i = m * kThreads + tid;
-      w[m] = i < nw ? __ldcg(&win[i]) : 0ull;
-    }
-    const uint32_t S = (nw + kParts - 1) / kParts;
-    if (tid <= kParts) cuts_s[tid] = nw;
-    const uint4 *hg = reinterpret_cast<const uint4 *>(ws.hist12 + static_cast<int64_t>(r) * kHistBins);
-    for (int i = tid; i < kHistBins / 4; i += kThreads) reinterpret_cast<uint4 *>(hs)[i] = __ldcg(&hg[i]);
+    for (uint32_t i = tid; i < nw; i += kThreads) sel[i] = __ldcg(&win[i]);
     __syncthreads();
-    constexpr int per = kHistBins / kThreads;    // this thread's bins, highest first
-    uint32_t c[per], sum = 0u;
-#pragma unroll
-    for (int m = 0; m < per; ++m) {
-      c[m] = hs[kHistBins - 1 - (tid * per + m)];
-      sum += c[m];
-    }
-    uint32_t total;
-    uint32_t run = block_excl_scan(sum, scratch, &total);   // its barriers end the reads of the counts
-#pragma unroll
-    for (int m = 0; m < per; ++m) {
-      const int b = kHistBins - 1 - (tid * per + m);
-      hs[b] = run;
-      if ((T == kNoBin || static_cast<uint32_t>(b) > T) && run < nw && c[m] > 0u)
-        for (int q = 1; q < kParts; ++q)
-          if (run >= q * S) atomicMin(&cuts_s[q], run);
-      run += c[m];
-    }
-    __syncthreads();
-    uint32_t s0 = 0u, s1 = nw;
-    {
-      uint32_t prev = 0u;
-      for (int q = 1; q <= part + 1; ++q) {
-        const uint32_t cq = q <= kParts - 1 ? max(cuts_s[q], prev) : nw;
-        if (q == part) s0 = cq;
-        if (q == part + 1) s1 = cq;
-        prev = cq;
-      }
-      if (part == 0) s0 = 0u;
-    }
-    if (s1 <= s0) return;   // uniform: an empty segment
-    if (tid == 0) count_s = 0u;
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < kSortCap / kThreads; ++m) {
-      const uint32_t i = m * kThreads + tid;
-      bool take = false;
-      if (i < nw) {
-        const uint32_t o = hs[static_cast<uint32_t>(w[m] >> 52)];
-        take = o >= s0 && o < s1;
-      }
-      warp_push64(take, w[m], sel, &count_s, static_cast<uint32_t>(kSortCap));
-    }
-    __syncthreads();
-    const int n = min(static_cast<int>(count_s), static_cast<int>(s1 - s0));
-    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand + kHistBins / 2, n, bstart, bcur, scratch);
-    for (int i = tid; i < n; i += kThreads)
-      out[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
+    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, static_cast<int>(nw), bstart, bcur, scratch);
+    for (uint32_t i = tid; i < nw; i += kThreads)
+      out[i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
     return;
   }
 
@@ -886,7 +848,7 @@ cudaError_t launch_collect(const SelectArgs &a_in, cudaStream_t stream) {
   cfg.dynamicSmemBytes = kCollectSmemAlloc;
   cudaError_t e = cudaLaunchKernelEx(&cfg, collect_kernel, a);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(kParts + 1, a.R);
+  cfg.gridDim = dim3(2, a.R);   // per row: the winners' CTA and the candidates' CTA
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kFinishSmemAlloc;
   return cudaLaunchKernelEx(&cfg, finish_kernel, a);
