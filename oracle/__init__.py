@@ -69,6 +69,8 @@ def _bind(path: str):
     lib.oracle_radix_key.restype = ctypes.c_uint32
     lib.oracle_first_digit_hist.argtypes = [p, i64, p, i32, p]
     lib.oracle_first_digit_hist.restype = None
+    lib.oracle_top1.argtypes = [p, i64, i32, i64, p, p]
+    lib.oracle_top1.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     return lib
@@ -161,6 +163,16 @@ class Oracle:
         f = self.lib.oracle_radix_key
         return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint32).reshape(x.shape)
 
+    def top1(self, logits_f32):
+        """(index, value) of each row's largest logit: ties to the lowest index,
+        NaN read as -1e30."""
+        x = _c(logits_f32, np.float32)
+        R, V = x.shape
+        idx = np.empty(R, dtype=np.int32)
+        val = np.empty(R, dtype=np.float32)
+        self.lib.oracle_top1(_ptr(x), V, R, V, _ptr(idx), _ptr(val))
+        return idx, val
+
     def first_digit_hist(self, scores_f32, row_bound) -> np.ndarray:
         s = _c(scores_f32, np.float32)
         rb = _c(row_bound, np.int32)
@@ -220,6 +232,10 @@ def topk(scores_f32, row_bound, K):
 
 def radix_key(x):
     return default().radix_key(x)
+
+
+def top1(logits_f32):
+    return default().top1(logits_f32)
 
 
 def first_digit_hist(scores_f32, row_bound):

@@ -273,6 +273,27 @@ void oracle_first_digit_hist(const float *scores, int64_t ld, const int32_t *row
     }
 }
 
+/* Top-1 of each row of logits (the sglang PR 48224 page, later commit
+ * "draft_topk1_postprocess"): the largest value, ties to the lowest index, a NaN
+ * read as -1e30.  out_idx [R] gets the index, out_val [R] the value as read.
+ * Values compare as floats, so -0.0 and +0.0 tie.  V >= 1. */
+void oracle_top1(const float *logits, int64_t ld, int R, int64_t V, int32_t *out_idx, float *out_val) {
+    for (int r = 0; r < R; ++r) {
+        const float *row = logits + (int64_t)r * ld;
+        int64_t best = 0;
+        float bv = isnan(row[0]) ? -1e30f : row[0];
+        for (int64_t j = 1; j < V; ++j) {
+            const float v = isnan(row[j]) ? -1e30f : row[j];
+            if (v > bv) {
+                bv = v;
+                best = j;
+            }
+        }
+        out_idx[r] = (int32_t)best;
+        out_val[r] = bv;
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

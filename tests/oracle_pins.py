@@ -364,6 +364,38 @@ def pin_first_digit_hist(orc):
         assert np.array_equal(hist[r], np.bincount(np.array(digits, dtype=np.int64), minlength=64))
 
 
+def _top1_by_definition(row):
+    """The top-1 by its statement, with Python's max: the largest value, NaN read as
+    -1e30, the lowest index among equal values (max over (value, -index))."""
+    vals = [(-1e30 if np.isnan(v) else float(v)) for v in row]
+    j = max(range(len(vals)), key=lambda i: (vals[i], -i))
+    return j, vals[j]
+
+
+def pin_top1_bruteforce(orc):
+    rng = np.random.default_rng(21)
+    x = rng.integers(-4, 5, size=(40, 37)).astype(np.float32)    # many ties
+    x[::7, 3] = np.nan
+    idx, val = orc.top1(x)
+    for r in range(x.shape[0]):
+        j, v = _top1_by_definition(x[r])
+        assert idx[r] == j and np.float32(val[r]) == np.float32(v), (r, idx[r], j)
+
+
+def pin_top1_special_values(orc):
+    rows = np.array([
+        [np.nan, np.nan, np.nan, np.nan],            # all NaN: index 0, value -1e30
+        [-np.inf, np.nan, -1e31, -np.inf],           # NaN (-1e30) beats -inf and -1e31
+        [-0.0, 0.0, -1.0, -0.0],                     # -0.0 and +0.0 tie: index 0
+        [1.0, np.inf, 3.0, np.inf],                  # +inf, lowest index
+        [-1e30, np.nan, -2e30, -1e30],               # NaN ties with -1e30: index 0
+    ], np.float32)
+    idx, val = orc.top1(rows)
+    assert list(idx) == [0, 1, 0, 1, 0], list(idx)
+    assert val[0] == np.float32(-1e30) and val[1] == np.float32(-1e30) and val[2] == 0.0
+    assert np.isinf(val[3]) and val[3] > 0 and val[4] == np.float32(-1e30)
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e4m3_closed_forms, pin_bf16_decode,
     pin_long_page_table, pin_page_table_scale_and_bound,
@@ -371,4 +403,5 @@ ALL_PINS = [
     pin_row_to_request, pin_bf16_cache, pin_einsum_scorer,
     pin_score_points, pin_topk_bruteforce, pin_topk_exhaustive_small, pin_topk_invariants,
     pin_topk_padding, pin_radix_key_monotone, pin_radix_first_digit, pin_first_digit_hist,
+    pin_top1_bruteforce, pin_top1_special_values,
 ]

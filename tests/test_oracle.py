@@ -43,6 +43,9 @@ MUTATIONS = [
     ("radix_negative", "return (u >> 31) ? ~u : (u | 0x80000000u);", "return (u >> 31) ? u : (u | 0x80000000u);"),
     ("negative_zero", "if (x == 0.0f) x = 0.0f;", ""),
     ("digit_shift", "oracle_radix_key(scores[(int64_t)r * ld + t]) >> 26", "oracle_radix_key(scores[(int64_t)r * ld + t]) >> 25 & 63"),
+    ("top1_ties_high_index", "if (v > bv) {", "if (v >= bv) {"),
+    ("top1_nan_kept", "const float v = isnan(row[j]) ? -1e30f : row[j];", "const float v = row[j];"),
+    ("top1_first_nan_kept", "float bv = isnan(row[0]) ? -1e30f : row[0];", "float bv = row[0];"),
 ]
 
 
