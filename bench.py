@@ -245,6 +245,55 @@ def emit(line, rank: int):
         print(json.dumps(line), flush=True)
 
 
+def run_top1(args):
+    """--op top1: the one-launch top-1 of R rows of V fp32 logits (the page's later
+    draft_topk1_postprocess commit), timed like the indexer launch: L2 flushed
+    before every step, CUDA events around the launch.  HBM-bound: R * V * 4 bytes."""
+    import numpy as np
+    import torch
+    import sparse_attention_indexer_launch_gb300 as lib
+    R, V = args.top1_rows, args.top1_vocab
+    rng = np.random.default_rng(11)
+    x = torch.from_numpy((rng.standard_normal((R, V)) * 4).astype(np.float32)).cuda()
+    idx = torch.empty(R, dtype=torch.int32, device="cuda")
+    state = torch.zeros(lib.top1_state_size(R), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        lib.idx_top1(x, idx, state)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        lib.idx_top1(x, idx, state)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    import oracle
+    xh = x.cpu().numpy()
+    ref, _ = oracle.top1(xh)
+    if not np.array_equal(ref, idx.cpu().numpy()):
+        raise SystemExit("idx_top1 result differs from the oracle")
+    t0 = time.perf_counter()
+    oracle.top1(xh)
+    cpu_s = time.perf_counter() - t0
+    hbm_gbs, _, peak_src = measured_peaks()
+    nbytes = R * V * 4
+    print(json.dumps({
+        "metric": "µs per top-1 launch (R rows x V fp32 logits)", "op": "top1", "value": us, "unit": "µs",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "config": {"workload": f"{R} rows x {V} logits, N(0, 16) fp32", "l2": "flushed before every step (256 MB write)"},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e-6) / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": nbytes / (us * 1e-6) / 1e9 / hbm_gbs, "algorithmic_bytes": nbytes,
+                     "peak_source": peak_src},
+        "cpu_baseline": {"value": cpu_s * 1e6, "unit": "µs", "cores": 1, "kind": "oracle",
+                         "sample": "the same rows, one pass of the oracle's loop"},
+    }))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -256,12 +305,18 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds for the whole --impl reference run")
+    ap.add_argument("--op", default="indexer", choices=["indexer", "top1"],
+                    help="indexer: the fused indexer launch (the benchmark); top1: the one-launch top-1")
+    ap.add_argument("--top1-rows", type=int, default=8)
+    ap.add_argument("--top1-vocab", type=int, default=151552)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not os.environ.get("IDX_BENCH_ALLOW_SHORT"):
         print("note: warm-up raised to 3 steps", file=sys.stderr)
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "top1":
+        return run_top1(args)
 
     import numpy as np
     import torch

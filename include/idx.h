@@ -158,6 +158,28 @@ int64_t idx_debug_set(int32_t what, int64_t value);
  * cudaEventElapsedTime.  Applies to one call, then clears itself.  Process-wide. */
 void idx_profile_events(void *start, void *stop);
 
+/* Top-1 of each row of logits in one launch: the later "draft_topk1_postprocess"
+ * commit on the sglang PR 48224 page.  Each split of a row folds its (value,
+ * lowest index) into a per-row 64-bit key with an atomic maximum; the split that
+ * arrives last writes the row's results and resets the row's state.  Ties go to
+ * the lowest index; a NaN reads as -1e30; -0.0 and +0.0 compare equal.
+ *   logits     device fp32 [R][ld], columns 0 .. V-1 read; ld >= V >= 1.
+ *   out_idx    device int32 [R]: the index of each row's largest value.
+ *   out_val    device fp32 [R] or NULL: that value (after the NaN reading; a zero
+ *              maximum is written as +0.0).
+ *   tokens     device int32 [R][tokens_ld] or NULL: tokens[r * tokens_ld + token_col]
+ *              gets out_idx[r] (the draft token column); 0 <= token_col < tokens_ld.
+ *   positions  device int32 [R] or NULL: positions[r] += 1.
+ *   state      device buffer of state_bytes >= idx_top1_state_size(R), 16-byte
+ *              aligned, all zero before its first use; every call leaves it zero
+ *              again.  Calls that share a state must not overlap in time.
+ * Returns IDX_EINVAL for a bad argument and IDX_EUNSUPPORTED for V > INT32_MAX, in
+ * both cases launching nothing. */
+size_t idx_top1_state_size(int32_t R);
+idx_status idx_top1(const float *logits, int64_t ld, int32_t R, int64_t V, int32_t *out_idx,
+                    float *out_val, int32_t *tokens, int64_t tokens_ld, int32_t token_col,
+                    int32_t *positions, void *state, size_t state_bytes, void *stream);
+
 /* Exact top-K of given scores with no caller workspace.  The page has no
  * counterpart: this is idx_topk run on scratch that lives in the library itself,
  * a file-scope device array of IDX_NOALLOC_SCRATCH_BYTES (enough for up to

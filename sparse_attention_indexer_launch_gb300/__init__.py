@@ -24,7 +24,7 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
-           "idx_debug_set", "idx_profile_events", "idx_topk_noalloc"]
+           "idx_debug_set", "idx_profile_events", "idx_top1_state_size", "idx_top1", "idx_topk_noalloc"]
 
 
 class IdxError(RuntimeError):
@@ -73,6 +73,10 @@ def _load():
     lib.idx_debug_set.restype = i64
     lib.idx_profile_events.argtypes = [vp, vp]
     lib.idx_profile_events.restype = None
+    lib.idx_top1_state_size.argtypes = [i32]
+    lib.idx_top1_state_size.restype = sz
+    lib.idx_top1.argtypes = [vp, i64, i32, i64, vp, vp, vp, i64, i32, vp, vp, sz, vp]
+    lib.idx_top1.restype = ctypes.c_int
     lib.idx_topk_noalloc.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp]
     lib.idx_topk_noalloc.restype = ctypes.c_int
     return lib
@@ -131,6 +135,22 @@ def idx_topk(scores, ld: int, row_bound, R: int, max_bound: int, K: int, hist, o
     _check(lib.idx_topk(_ptr(scores), int(ld), _ptr(row_bound), int(R), int(max_bound), int(K),
                         _ptr(hist), _ptr(out_idx), _ptr(ws), ws.numel() * ws.element_size(),
                         _stream(stream)), "idx_topk")
+
+
+def top1_state_size(R: int) -> int:
+    return int(lib.idx_top1_state_size(int(R)))
+
+
+def idx_top1(logits, out_idx, state, out_val=None, tokens=None, token_col: int = 0, positions=None,
+             V: int | None = None, stream=None):
+    """Top-1 of each row of a [R][ld] fp32 tensor (see idx.h); `state` is a zeroed
+    uint8 device tensor of top1_state_size(R) bytes, left zero by every call."""
+    R, ld = int(logits.shape[0]), int(logits.stride(0))
+    V = int(V if V is not None else logits.shape[1])
+    tokens_ld = int(tokens.stride(0)) if tokens is not None else 0
+    _check(lib.idx_top1(_ptr(logits), ld, R, V, _ptr(out_idx), _ptr(out_val), _ptr(tokens), tokens_ld,
+                        int(token_col), _ptr(positions), _ptr(state), state.numel() * state.element_size(),
+                        _stream(stream)), "idx_top1")
 
 
 def idx_topk_noalloc(scores, ld: int, row_bound, R: int, max_bound: int, K: int, out_idx, stream=None):

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <climits>
 #include <mutex>
 
 #include "idx.h"
@@ -418,6 +419,37 @@ int64_t idx_debug_set(int32_t what, int64_t value) {
     g_stall_next = value > 0 ? value : 0;
   }
   return prev;
+}
+
+size_t idx_top1_state_size(int32_t R) {
+  return R < 1 ? 0 : static_cast<size_t>(R) * sizeof(idx::Top1State);
+}
+
+idx_status idx_top1(const float *logits, int64_t ld, int32_t R, int64_t V, int32_t *out_idx, float *out_val,
+                    int32_t *tokens, int64_t tokens_ld, int32_t token_col, int32_t *positions, void *state,
+                    size_t state_bytes, void *stream) {
+  if (logits == nullptr || out_idx == nullptr || state == nullptr) return IDX_EINVAL;
+  if (R < 1 || V < 1 || ld < V) return IDX_EINVAL;
+  if (V > INT32_MAX || R > IDX_MAX_ROWS) return IDX_EUNSUPPORTED;
+  if (tokens != nullptr && (tokens_ld < 1 || token_col < 0 || token_col >= tokens_ld)) return IDX_EINVAL;
+  if (state_bytes < idx_top1_state_size(R) || (reinterpret_cast<uintptr_t>(state) & 15u) != 0) return IDX_EINVAL;
+  int sms = 0;
+  idx_status st = device_sms(&sms);
+  if (st != IDX_OK) return st;
+  idx::Top1Args t{};
+  t.logits = logits;
+  t.ld = ld;
+  t.V = V;
+  t.R = R;
+  t.out_idx = out_idx;
+  t.out_val = out_val;
+  t.tokens = tokens;
+  t.tokens_ld = tokens_ld;
+  t.token_col = token_col;
+  t.positions = positions;
+  t.state = static_cast<idx::Top1State *>(state);
+  t.vec4 = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && ld % 4 == 0;
+  return cuda_ok(idx::launch_top1(t, sms, static_cast<cudaStream_t>(stream)));
 }
 
 idx_status idx_topk_noalloc(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R,

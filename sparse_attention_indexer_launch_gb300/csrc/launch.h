@@ -45,6 +45,27 @@ struct SelectArgs {
   int32_t slice;           // keys per collect CTA (set by launch_collect)
 };
 
+struct Top1State {          // per row, zero between calls
+  unsigned long long key;  // running maximum of (radix_key(value) << 32) | ~index
+  uint32_t arrived;        // splits of the row that have folded in their maximum
+  uint32_t pad;
+};
+
+struct Top1Args {
+  const float *logits;
+  int64_t ld, V;
+  int32_t R;
+  int32_t *out_idx;
+  float *out_val;          // or null
+  int32_t *tokens;         // or null: tokens[r * tokens_ld + token_col]
+  int64_t tokens_ld;
+  int32_t token_col;
+  int32_t *positions;      // or null: positions[r] += 1
+  Top1State *state;        // [R]
+  int64_t chunk;           // values per split (set by launch_top1)
+  int32_t vec4;            // rows and chunks allow 16-byte loads
+};
+
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
 cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
                          cudaStream_t stream);
@@ -53,5 +74,7 @@ cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dty
 cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, cudaStream_t stream);
 cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream);
+// Top-1 of each row of logits (one launch: splits and last-arriver finalize).
+cudaError_t launch_top1(const Top1Args &a, int num_sms, cudaStream_t stream);
 
 }  // namespace idx

@@ -20,7 +20,7 @@ def idxlib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "idx.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(idx_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(idx_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -86,3 +86,18 @@ def test_debug_hooks_roundtrip(idxlib):
     prev = idxlib.debug_set(idxlib.IDX_DEBUG_WAIT_LIMIT_NS, 12345)
     assert idxlib.debug_set(idxlib.IDX_DEBUG_WAIT_LIMIT_NS, prev) == 12345
     assert idxlib.debug_set(idxlib.IDX_DEBUG_STALL_SCORE_MMA, 0) == 0
+
+
+def test_top1_rejects_bad_arguments_without_a_gpu(idxlib):
+    lib = idxlib.lib
+    st = 0x10000
+    assert lib.idx_top1_state_size(8) == 8 * 16 and lib.idx_top1_state_size(0) == 0
+    # null logits, V < 1, ld < V, small state, misaligned state, bad token column
+    assert lib.idx_top1(None, 10, 2, 10, 0x20000, None, None, 0, 0, None, st, 64, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 10, 2, 0, 0x20000, None, None, 0, 0, None, st, 64, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 5, 2, 10, 0x20000, None, None, 0, 0, None, st, 64, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 10, 2, 10, 0x20000, None, None, 0, 0, None, st, 16, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 10, 2, 10, 0x20000, None, None, 0, 0, None, st + 4, 64, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 10, 2, 10, 0x20000, None, 0x40000, 4, 4, None, st, 64, None) == idxlib.IDX_EINVAL
+    assert lib.idx_top1(0x30000, 1 << 32, 2, 1 << 32, 0x20000, None, None, 0, 0, None, st, 64, None) \
+        == idxlib.IDX_EUNSUPPORTED
