@@ -69,6 +69,10 @@ def _bind(path: str):
     lib.oracle_radix_key.restype = ctypes.c_uint32
     lib.oracle_first_digit_hist.argtypes = [p, i64, p, i32, p]
     lib.oracle_first_digit_hist.restype = None
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_quantize_key.argtypes = [p, p, p]
+    lib.oracle_quantize_key.restype = None
     lib.oracle_top1.argtypes = [p, i64, i32, i64, p, p]
     lib.oracle_top1.restype = None
     lib.oracle_num_threads.argtypes = []
@@ -162,6 +166,40 @@ class Oracle:
         x = np.asarray(x, dtype=np.float32)
         f = self.lib.oracle_radix_key
         return np.array([f(float(v)) for v in x.ravel()], dtype=np.uint32).reshape(x.shape)
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        x = np.asarray(x, dtype=np.float32).ravel()
+        return np.array([self.lib.oracle_e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+
+    def quantize_key(self, key_bf16_bits):
+        """(E4M3 codes [128], fp32 scale) of one key given as bf16 bit patterns."""
+        k = _c(key_bf16_bits, np.uint16)
+        codes = np.empty(128, dtype=np.uint8)
+        sc = np.empty(1, dtype=np.float32)
+        self.lib.oracle_quantize_key(_ptr(k), _ptr(codes), _ptr(sc))
+        return codes, np.float32(sc[0])
+
+    def patch_new_keys(self, prob, k_new_bits):
+        """A copy of prob with every row's new key written at its position
+        row_bound - 1 (rows with bound 0 write nothing): E4M3 codes and scale, or
+        the bf16 values for a bf16 cache."""
+        import copy
+        out = copy.copy(prob)
+        out.k_cache = prob.k_cache.copy()
+        out.k_scale = None if prob.k_scale is None else prob.k_scale.copy()
+        for r in range(prob.R):
+            b = int(prob.row_bound[r])
+            if b <= 0:
+                continue
+            t = b - 1
+            page = int(prob.page_table[prob.row_req[r], t // 64])
+            if prob.kv_dtype == "e4m3":
+                codes, sc = self.quantize_key(k_new_bits[r])
+                out.k_cache[page, t % 64] = codes
+                out.k_scale[page, t % 64] = sc
+            else:
+                out.k_cache[page, t % 64] = k_new_bits[r]
+        return out
 
     def top1(self, logits_f32):
         """(index, value) of each row's largest logit: ties to the lowest index,

@@ -64,6 +64,44 @@ double oracle_e4m3_to_double(uint8_t code) {
     return sign ? -magnitude : magnitude;
 }
 
+double oracle_bf16_to_double(uint16_t bits);
+
+/* The E4M3 code nearest to x (ties to an even mantissa), from the format above:
+ * |x| is first clamped to the largest finite value 448; below 2^-6 the step is the
+ * subnormal one, 2^-9.  Every step is exact in double. */
+uint8_t oracle_e4m3_encode(float x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a > 448.0) a = 448.0;
+    if (a < ldexp(1.0, -6)) {                       /* subnormal range: m * 2^-9, m in 0..8 */
+        const double m = rint(ldexp(a, 9));         /* m == 8 is the smallest normal, 2^-6 */
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int e = ilogb(a);                               /* a = f * 2^e, 1 <= f < 2 */
+    double m = rint(ldexp(a, 3 - e));               /* 8 .. 16 */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)m - 8));
+}
+
+/* The new key of a decode row, as the launch writes it into the paged cache (the
+ * later commit "New keys, as #74 has them" on the page: a key this launch writes
+ * is scored for every row of its request).  E4M3 cache: scale = amax / 448 in fp32
+ * (1 for a zero key), each value x / scale in fp32, clamped to +-448, encoded to
+ * the nearest E4M3 code.  bf16 cache: the values as given.  key_bf16 [128]. */
+void oracle_quantize_key(const uint16_t *key_bf16, uint8_t *codes, float *scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < ORACLE_DIM; ++i) {
+        const float v = fabsf((float)oracle_bf16_to_double(key_bf16[i]));
+        if (v > amax) amax = v;
+    }
+    const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < ORACLE_DIM; ++i) codes[i] = oracle_e4m3_encode((float)oracle_bf16_to_double(key_bf16[i]) / sc);
+    *scale = sc;
+}
+
 /* bfloat16: the upper 16 bits of an IEEE binary32. */
 double oracle_bf16_to_double(uint16_t bits) {
     uint32_t wide = ((uint32_t)bits) << 16;

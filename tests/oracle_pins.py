@@ -396,6 +396,62 @@ def pin_top1_special_values(orc):
     assert np.isinf(val[3]) and val[3] > 0 and val[4] == np.float32(-1e30)
 
 
+def _lib_e4m3(x):
+    """Library encoder: torch's float8_e4m3fn cast (round to nearest even) after
+    clamping to the largest finite value."""
+    x = np.clip(np.asarray(x, dtype=np.float32), -448.0, 448.0)
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_encode_vs_library(orc):
+    rng = np.random.default_rng(31)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = orc.e4m3_to_double(finite).astype(np.float32)
+    pos = np.sort(vals[vals > 0])
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)     # exact ties
+    rand = (rng.choice([-1, 1], 4000) * np.exp(rng.uniform(np.log(1e-5), np.log(1e3), 4000))).astype(np.float32)
+    x = np.concatenate([vals, mids, -mids, rand, np.array([0.0, -0.0, 448.0, 449.0, 1e9, -1e9], np.float32)])
+    assert np.array_equal(orc.e4m3_encode(x), _lib_e4m3(x))
+
+
+def pin_e4m3_encode_roundtrip(orc):
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    back = orc.e4m3_encode(orc.e4m3_to_double(codes).astype(np.float32))
+    assert np.array_equal(back, codes)
+
+
+def pin_quantize_key(orc):
+    rng = np.random.default_rng(32)
+    for amp in (1.0, 1e-4, 300.0):
+        x = (rng.standard_normal(128) * amp).astype(np.float32)
+        bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+        scale = np.float32(np.abs(xb).max()) / np.float32(448.0)
+        codes, sc = orc.quantize_key(bits)
+        assert sc == scale
+        assert np.array_equal(codes, _lib_e4m3(xb / scale))
+        assert codes[np.argmax(np.abs(xb))] & 0x7F == 126          # the largest value maps to +-448
+    codes, sc = orc.quantize_key(np.zeros(128, np.uint16))
+    assert sc == np.float32(1.0) and not codes.any()
+
+
+def pin_patch_position(orc):
+    prob = workloads.build("patch", [300, 130], [2, 1], "e4m3", seed=33)
+    rng = np.random.default_rng(34)
+    k_new = torch.from_numpy(rng.standard_normal((prob.R, 128)).astype(np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    out = orc.patch_new_keys(prob, k_new)
+    changed = np.argwhere((out.k_cache != prob.k_cache).any(axis=2))
+    expect = set()
+    for r in range(prob.R):
+        t = int(prob.row_bound[r]) - 1
+        page = int(prob.page_table[prob.row_req[r], t // 64])
+        expect.add((page, t % 64))
+        codes, sc = orc.quantize_key(k_new[r])
+        assert np.array_equal(out.k_cache[page, t % 64], codes) and out.k_scale[page, t % 64] == sc
+    assert set(map(tuple, changed.tolist())) <= expect
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e4m3_closed_forms, pin_bf16_decode,
     pin_long_page_table, pin_page_table_scale_and_bound,
@@ -404,4 +460,5 @@ ALL_PINS = [
     pin_score_points, pin_topk_bruteforce, pin_topk_exhaustive_small, pin_topk_invariants,
     pin_topk_padding, pin_radix_key_monotone, pin_radix_first_digit, pin_first_digit_hist,
     pin_top1_bruteforce, pin_top1_special_values,
+    pin_e4m3_encode_vs_library, pin_e4m3_encode_roundtrip, pin_quantize_key, pin_patch_position,
 ]

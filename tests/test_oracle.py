@@ -46,6 +46,10 @@ MUTATIONS = [
     ("top1_ties_high_index", "if (v > bv) {", "if (v >= bv) {"),
     ("top1_nan_kept", "const float v = isnan(row[j]) ? -1e30f : row[j];", "const float v = row[j];"),
     ("top1_first_nan_kept", "float bv = isnan(row[0]) ? -1e30f : row[0];", "float bv = row[0];"),
+    ("encode_truncates", "double m = rint(ldexp(a, 3 - e));", "double m = floor(ldexp(a, 3 - e));"),
+    ("encode_bias", "(uint8_t)((e + 7) << 3)", "(uint8_t)((e + 8) << 3)"),
+    ("encode_subnormal_step", "const double m = rint(ldexp(a, 9));", "const double m = rint(ldexp(a, 8));"),
+    ("key_scale_unscaled", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float sc = amax > 0.0f ? amax : 1.0f;"),
 ]
 
 
