@@ -294,6 +294,51 @@ def run_top1(args):
     return 0
 
 
+def run_patch(args):
+    """--op patch: idx_patch_new_keys on the benchmark workload (8 rows' new keys
+    quantised and written into the paged cache), CUDA events around the call."""
+    import numpy as np
+    import torch
+    import sparse_attention_indexer_launch_gb300 as lib
+    import workloads
+    prob = workloads.make_config(3)
+    dp = lib.DeviceProblem(prob)
+    rng = np.random.default_rng(12)
+    k_new = torch.from_numpy(rng.standard_normal((prob.R, 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        lib.idx_patch_new_keys(dp.problem, k_new)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        lib.idx_patch_new_keys(dp.problem, k_new)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us_call = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    # the same call replayed from a CUDA graph: the device time without the host's
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        lib.idx_patch_new_keys(dp.problem, k_new)
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lib.idx_patch_new_keys(dp.problem, k_new)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    print(json.dumps({"metric": "µs per new-key patch (8 rows, E4M3 cache), CUDA-graph replay", "op": "patch",
+                      "value": us, "us_per_call_from_python": us_call,
+                      "unit": "µs", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+                      "warmup": args.warmup, "config": {"workload": workloads.CONFIG_NAMES[3]}}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -305,8 +350,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds for the whole --impl reference run")
-    ap.add_argument("--op", default="indexer", choices=["indexer", "top1"],
-                    help="indexer: the fused indexer launch (the benchmark); top1: the one-launch top-1")
+    ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch"],
+                    help="indexer: the fused indexer launch (the benchmark); top1: the one-launch top-1; "
+                         "patch: the new-key patch")
     ap.add_argument("--top1-rows", type=int, default=8)
     ap.add_argument("--top1-vocab", type=int, default=151552)
     args = ap.parse_args()
@@ -317,6 +363,8 @@ def main():
         return run_reference(args)
     if args.op == "top1":
         return run_top1(args)
+    if args.op == "patch":
+        return run_patch(args)
 
     import numpy as np
     import torch

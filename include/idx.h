@@ -158,6 +158,22 @@ int64_t idx_debug_set(int32_t what, int64_t value);
  * cudaEventElapsedTime.  Applies to one call, then clears itself.  Process-wide. */
 void idx_profile_events(void *start, void *stop);
 
+/* Writes every row's new key into the paged cache, ahead of idx_launch (the sglang
+ * PR 48224 page, section Reviewer notes, "New keys": a key the launch writes is
+ * scored for every row of its request in the launch).  Row r's key goes to logical
+ * position row_bound[r] - 1 of request row_req[r], so the scan that follows reads it
+ * for every row whose bound covers it.
+ *   problem  as for idx_launch; problem->k_cache and problem->k_scale are WRITTEN
+ *            (device memory the caller owns and may write).
+ *   k_new    device bf16 [R][128], 16-byte aligned: each row's new key.
+ * E4M3 cache: scale = amax / 448 in fp32 (1 for a zero key) goes to k_scale, and
+ * each value divided by it in fp32 goes to the nearest E4M3 code (ties to even),
+ * saturating at +-448.  bf16 cache: the values as given.  Rows with bound 0 write
+ * nothing; a row whose page id is outside [0, P) writes nothing (idx_launch then
+ * reports the page).  Rows of one request must have different bounds (each writes
+ * its own position).  Asynchronous on `stream`; allocates nothing. */
+idx_status idx_patch_new_keys(const idx_problem *problem, const void *k_new, void *stream);
+
 /* Top-1 of each row of logits in one launch: the later "draft_topk1_postprocess"
  * commit on the sglang PR 48224 page.  Each split of a row folds its (value,
  * lowest index) into a per-row 64-bit key with an atomic maximum; the split that

@@ -24,7 +24,8 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
-           "idx_debug_set", "idx_profile_events", "idx_top1_state_size", "idx_top1", "idx_topk_noalloc"]
+           "idx_debug_set", "idx_profile_events", "idx_top1_state_size", "idx_top1", "idx_topk_noalloc",
+           "idx_patch_new_keys"]
 
 
 class IdxError(RuntimeError):
@@ -73,6 +74,8 @@ def _load():
     lib.idx_debug_set.restype = i64
     lib.idx_profile_events.argtypes = [vp, vp]
     lib.idx_profile_events.restype = None
+    lib.idx_patch_new_keys.argtypes = [P, vp, vp]
+    lib.idx_patch_new_keys.restype = ctypes.c_int
     lib.idx_top1_state_size.argtypes = [i32]
     lib.idx_top1_state_size.restype = sz
     lib.idx_top1.argtypes = [vp, i64, i32, i64, vp, vp, vp, i64, i32, vp, vp, sz, vp]
@@ -135,6 +138,12 @@ def idx_topk(scores, ld: int, row_bound, R: int, max_bound: int, K: int, hist, o
     _check(lib.idx_topk(_ptr(scores), int(ld), _ptr(row_bound), int(R), int(max_bound), int(K),
                         _ptr(hist), _ptr(out_idx), _ptr(ws), ws.numel() * ws.element_size(),
                         _stream(stream)), "idx_topk")
+
+
+def idx_patch_new_keys(problem: Problem, k_new, stream=None):
+    """Writes each row's new key (bf16 [R][128] device tensor) into the problem's
+    cache at position row_bound - 1 (see idx.h)."""
+    _check(lib.idx_patch_new_keys(ctypes.byref(problem), _ptr(k_new), _stream(stream)), "idx_patch_new_keys")
 
 
 def top1_state_size(R: int) -> int:

@@ -421,6 +421,25 @@ int64_t idx_debug_set(int32_t what, int64_t value) {
   return prev;
 }
 
+idx_status idx_patch_new_keys(const idx_problem *problem, const void *k_new, void *stream) {
+  idx_status st = check_problem(problem);
+  if (st != IDX_OK) return st;
+  if (k_new == nullptr || (reinterpret_cast<uintptr_t>(k_new) & 15u) != 0) return IDX_EINVAL;
+  idx::PatchArgs pa{};
+  pa.k_new = static_cast<const uint16_t *>(k_new);
+  pa.row_req = problem->row_req;
+  pa.row_bound = problem->row_bound;
+  pa.page_table = problem->page_table;
+  pa.k_cache = const_cast<void *>(problem->k_cache);
+  pa.k_scale = const_cast<float *>(problem->k_scale);
+  pa.R = problem->R;
+  pa.Q = problem->Q;
+  pa.pt_stride = problem->pt_stride;
+  pa.kv_dtype = problem->kv_dtype;
+  pa.P = problem->P;
+  return cuda_ok(idx::launch_patch(pa, static_cast<cudaStream_t>(stream)));
+}
+
 size_t idx_top1_state_size(int32_t R) {
   return R < 1 ? 0 : static_cast<size_t>(R) * sizeof(idx::Top1State);
 }

@@ -66,6 +66,15 @@ struct Top1Args {
   int32_t vec4;            // rows and chunks allow 16-byte loads
 };
 
+struct PatchArgs {
+  const uint16_t *k_new;   // bf16 [R][128]
+  const int32_t *row_req, *row_bound, *page_table;
+  void *k_cache;           // E4M3 bytes or bf16 [P][64][128]
+  float *k_scale;          // [P][64] for E4M3
+  int32_t R, Q, pt_stride, kv_dtype;
+  int64_t P;
+};
+
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
 cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
                          cudaStream_t stream);
@@ -74,6 +83,8 @@ cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dty
 cudaError_t launch_select_clear(const SelectArgs &a, const int32_t *row_bound, cudaStream_t stream);
 cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream);
+// Every row's new key into the paged cache at position bound - 1.
+cudaError_t launch_patch(const PatchArgs &a, cudaStream_t stream);
 // Top-1 of each row of logits (one launch: splits and last-arriver finalize).
 cudaError_t launch_top1(const Top1Args &a, int num_sms, cudaStream_t stream);
 

@@ -101,3 +101,13 @@ def test_top1_rejects_bad_arguments_without_a_gpu(idxlib):
     assert lib.idx_top1(0x30000, 10, 2, 10, 0x20000, None, 0x40000, 4, 4, None, st, 64, None) == idxlib.IDX_EINVAL
     assert lib.idx_top1(0x30000, 1 << 32, 2, 1 << 32, 0x20000, None, None, 0, 0, None, st, 64, None) \
         == idxlib.IDX_EUNSUPPORTED
+
+
+def test_patch_rejects_bad_arguments_without_a_gpu(idxlib):
+    import ctypes as C
+    lib = idxlib.lib
+    prob = _fake_problem(idxlib)
+    assert lib.idx_patch_new_keys(C.byref(prob), None, None) == idxlib.IDX_EINVAL
+    assert lib.idx_patch_new_keys(C.byref(prob), 0x80008, None) == idxlib.IDX_EINVAL    # not 16-byte aligned
+    bad = _fake_problem(idxlib, R=0)
+    assert lib.idx_patch_new_keys(C.byref(bad), 0x80000, None) == idxlib.IDX_EINVAL
