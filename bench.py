@@ -345,7 +345,7 @@ def main():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="3", help="workload: 0..4 or 3a (default 3)")
+    ap.add_argument("--config", default="3", help="workload: 0..4, 3a or 3b (default 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=120.0,
@@ -380,7 +380,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    cfg = args.config if args.config == "3a" else int(args.config)
+    cfg = args.config if args.config in ("3a", "3b") else int(args.config)
     prob = rank_problem(cfg, rank)
     dp = lib.DeviceProblem(prob)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")

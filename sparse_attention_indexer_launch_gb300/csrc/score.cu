@@ -16,7 +16,8 @@
 //     D[key][row*64 + head] = <k_key, q_row_head>      (M = 128, N = 64 * rows)
 // so a TMEM lane holds one key and each epilogue thread reduces its key's 64
 // head values of a row in registers.
-//   warp 0      producer: page ids (32 per lane load, a block ahead), TMA of the
+//   warp 0      producer (with warp 18 for an E4M3 cache: even / odd tiles):
+//               page ids (32 per lane load, a block ahead), TMA of the
 //               key pages into an smem ring, the keys' scales into a second ring
 //               (cp.async by the warp's lanes), and the group's query operand
 //               (bulk copy) on group changes;
@@ -37,7 +38,9 @@ namespace idx {
 namespace {
 
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kProducers = 2;                  // producer warps for an E4M3 cache
+constexpr int kProducer2Warp = 2 + kEpiWarps;  // the second one, after the epilogue warps
+constexpr int kThreads = 64 + kEpiWarps * 32 + 32;
 constexpr int kBOperandBytes = 2 * kMaxGroupRows * kRowOperandBytes;  // two K blocks
 constexpr int kTmemCols = 512;                                        // two accumulators of 256
 constexpr int kScaleSlots = 8;
@@ -215,15 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   const uint64_t limit = a.wait_limit_ns;
   volatile int *abort = &bars->abort;
 
-  if (warp == 0) {
+  if (warp == 0 || (KV == IDX_KV_E4M3 && kProducers == 2 && warp == kProducer2Warp)) {
     // ------------------------------------------------------------------ producer
-    // The whole warp runs the loop: lanes hold the page ids of the current and
-    // next block of 16 tiles (32 pages, one lane each) and copy the tile's 128
-    // key scales (16 bytes per lane); lane 0 issues the key pages' TMA.
+    // E4M3: two producer warps, warp 0 for the even tiles of the CTA's range and
+    // warp kProducer2Warp for the odd ones (their key stages and scale slots are
+    // disjoint: both ring lengths are even); bf16: warp 0 alone.  In each, the whole
+    // warp runs the loop: lanes hold the page ids of the current and next block of
+    // 16 tiles (32 pages, one lane each) and copy the tile's 128 key scales (16 bytes
+    // per lane); lane 0 issues the key pages' TMA.  Warp 0 also loads the query
+    // operand of every group of the range, in order.
+    const int pp = warp == 0 ? 0 : 1;           // this producer's tile parity
+    const int np = KV == IDX_KV_E4M3 ? kProducers : 1;
     const uint64_t policy = l2_evict_first_policy();
     GroupCursor cur;
     cur.seek(ws.groups, num_groups, static_cast<int>(t0));
-    int cur_g = -1, req = 0, L = 0, nswitch = 0, tile_begin = 0;
+    int cur_g = -1, req = 0, L = 0, tile_begin = 0;
     int32_t blk_ids = -2, nxt_ids = -2;   // this lane's page id in the current / next block
     int blk = -1;                          // current block of 16 tiles within the group
     // Waits are taken by lane 0 and the outcome broadcast, so the lanes never split.
@@ -236,25 +245,45 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       const int64_t page = static_cast<int64_t>(b) * 32 + lane;
       return page * kPage < L ? a.page_table[static_cast<int64_t>(req) * a.pt_stride + page] : -2;
     };
-    int k = 0;
-    for (int64_t t = t0; t < t1; ++t, ++k) {
+    // warp 0: the query operand of every group with tiles in the range that starts
+    // at or before tile `upto`, in order (groups without tiles have none: the MMA
+    // issuer never switches to them)
+    int nb = 0;                                 // query operands loaded
+    int bg = cur.g;                             // next group to consider (seek lands on a group with tiles)
+    auto load_b_upto = [&](int64_t upto) -> bool {
+      while (bg < num_groups) {
+        const int begin = ws.groups[bg].tile_begin;
+        if (begin > upto || begin >= t1) break;
+        const int end = bg + 1 < num_groups ? ws.groups[bg + 1].tile_begin : total_tiles;
+        if (end > begin) {
+          if (nb > 0 && !warp_wait(&bars->bfree, (nb - 1) & 1)) return false;
+          if (lane == 0) {
+            const Group grp = ws.groups[bg];
+            const uint32_t bytes = grp.nrows * kRowOperandBytes;
+            mbar_arrive_expect_tx(&bars->bfull, 2 * bytes);
+            bulk_load(sB0, ws.qop0 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
+            bulk_load(sB1, ws.qop1 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
+          }
+          ++nb;
+        }
+        ++bg;
+      }
+      return true;
+    };
+    bool ok = true;
+    int last_k = -1;
+    for (int64_t t = t0 + pp; t < t1; t += np) {
+      const int k = static_cast<int>(t - t0);
+      if (pp == 0 && !load_b_upto(t)) {
+        ok = false;
+        break;
+      }
       if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
         const Group grp = ws.groups[cur.g];
-        if (cur_g >= 0 && !warp_wait(&bars->bfree, (nswitch - 1) & 1)) {
-          if (lane == 0) set_abort(bars, ws.status);
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t bytes = grp.nrows * kRowOperandBytes;
-          mbar_arrive_expect_tx(&bars->bfull, 2 * bytes);
-          bulk_load(sB0, ws.qop0 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
-          bulk_load(sB1, ws.qop1 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
-        }
         cur_g = cur.g;
         req = grp.req;
         L = grp.L;
         tile_begin = grp.tile_begin;
-        ++nswitch;
         blk = (static_cast<int>(t) - tile_begin) >> 4;
         blk_ids = block_ids(blk);
         nxt_ids = block_ids(blk + 1);
@@ -272,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       const int ss = k % kScaleSlots;
       if (!warp_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1) ||
           (KV == IDX_KV_E4M3 && !warp_wait(&bars->sempty[ss], ((k / kScaleSlots) & 1) ^ 1))) {
-        if (lane == 0) set_abort(bars, ws.status);
+        ok = false;
         break;
       }
       uint32_t bytes = 0;
@@ -308,23 +337,32 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
                      a.k_scale + static_cast<int64_t>(pages[h]) * kPage + (lane & 15) * 4);
         cp_async_arrive_noinc(&bars->sfull[ss]);
       }
+      last_k = k;
     }
-    // Wait for every copy still in flight before the CTA may exit (also after an abort).
+    if (ok && pp == 0) ok = load_b_upto(t1 - 1);   // groups whose tiles all fell to the other producer
+    if (!ok && lane == 0) set_abort(bars, ws.status);
+    // Wait for every copy this warp still has in flight before the CTA may exit (also
+    // after an abort): for each stage and scale slot, its last use by this warp.
     int never = 0;
-    const int issued = k;
-    for (int s = 0; s < C::kStages && s < issued; ++s) {
-      const int last_use = issued - 1 - ((issued - 1 - s) % C::kStages);
-      if (!mbar_wait(&bars->full[s], (last_use / C::kStages) & 1, limit, &never) && lane == 0)
+    auto last_use = [&](int slot, int ring) -> int {   // largest k <= last_k of this warp's parity
+      if (last_k < 0) return -1;
+      const int back = ((last_k - slot) % ring + ring) % ring;
+      const int kk = last_k - back;
+      return (kk >= 0 && (kk - pp) % np == 0) ? kk : -1;
+    };
+    for (int s = 0; s < C::kStages; ++s) {
+      const int lu = last_use(s, C::kStages);
+      if (lu >= 0 && !mbar_wait(&bars->full[s], (lu / C::kStages) & 1, limit, &never) && lane == 0)
         flag_status(ws.status, kStatusTimeout);
     }
     if (KV == IDX_KV_E4M3) {
-      for (int s = 0; s < kScaleSlots && s < issued; ++s) {
-        const int last_use = issued - 1 - ((issued - 1 - s) % kScaleSlots);
-        if (!mbar_wait(&bars->sfull[s], (last_use / kScaleSlots) & 1, limit, &never) && lane == 0)
+      for (int s = 0; s < kScaleSlots; ++s) {
+        const int lu = last_use(s, kScaleSlots);
+        if (lu >= 0 && !mbar_wait(&bars->sfull[s], (lu / kScaleSlots) & 1, limit, &never) && lane == 0)
           flag_status(ws.status, kStatusTimeout);
       }
     }
-    if (nswitch > 0 && !mbar_wait(&bars->bfull, (nswitch - 1) & 1, limit, &never) && lane == 0)
+    if (pp == 0 && nb > 0 && !mbar_wait(&bars->bfull, (nb - 1) & 1, limit, &never) && lane == 0)
       flag_status(ws.status, kStatusTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -377,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       int never = 0;
       if (!mbar_wait(&bars->drain, 0, limit, &never)) flag_status(ws.status, kStatusTimeout);
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------------ epilogue
     // Two groups of eight warps take alternate tiles (group g reads accumulator g);
     // within a group each warp reduces two rows of the tile for its TMEM lane quarter.

@@ -137,7 +137,7 @@ def test_topk_given_adversarial_scores(lib, orc):
         gpu_util.check_selection(orc, out.cpu().numpy(), s, bounds, K)
 
 
-@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4, "3b"])
 def test_configs_full_size(lib, orc, cfg):
     """The five workloads at full size: sampled scores, the fused histogram, exact
     selection on the GPU's scores, and the end-to-end rule against the oracle."""

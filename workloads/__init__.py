@@ -226,6 +226,7 @@ CONFIG_NAMES = {
     2: "cfg2: 8 requests x 4 rows, log-uniform 8K-256K keys, E4M3, shared shuffled pool",
     3: "cfg3: 2 requests x 4 rows, 524,288 keys each, E4M3, sigma 1/4 mixture keys",
     "3a": "cfg3a: 1 request x 4 rows, 524,288 keys, E4M3, sigma 1/4 mixture keys",
+    "3b": "cfg3b: 1 request x 1 row at 524,288 keys and 1 pad row (bound 0), E4M3, sigma 1/4 mixture keys",
     4: "cfg4: 64 requests x 1-4 rows, log-uniform 1K-512K keys, bf16 cache",
 }
 
@@ -255,6 +256,9 @@ def _make_config(cfg, off: int) -> Problem:
     if cfg == "3a":
         return build(CONFIG_NAMES["3a"], [524288], [4], "e4m3", seed=3 + off, key_dist="mixture",
                      recipe="first request of cfg3 alone")
+    if cfg == "3b":
+        return build(CONFIG_NAMES["3b"], [524288, 0], [1, 1], "e4m3", seed=3 + off, key_dist="mixture",
+                     recipe="cfg3's first request with one row, and a pad row of an empty request")
     if cfg == 4:
         rng = np.random.default_rng(1004)
         rows = [int(x) for x in rng.integers(1, 5, size=64)]
