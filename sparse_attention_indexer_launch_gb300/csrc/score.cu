@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       int cur_g = -1, nswitch = 0;
       uint32_t idesc = 0;
       const uint32_t fmt = KV == IDX_KV_E4M3 ? 0u : 1u;
+      const uint64_t bdesc0 = umma_desc_sw128(smem_u32(sB0)), bdesc1 = umma_desc_sw128(smem_u32(sB1));
       int k = 0;
       for (int64_t t = t0; t < t1; ++t, ++k) {
         cur.advance(static_cast<int>(t));
@@ -394,17 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * 256;
-        const uint32_t a_base = smem_u32(sA + s * C::kStageBytes);
-        const uint32_t b0 = smem_u32(sB0), b1 = smem_u32(sB1);
+        // descriptors of the K steps: the base descriptor plus the step's byte offset / 16
+        // (the start-address field holds address / 16; no carry out of it in 256 KB)
+        const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * C::kStageBytes));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
-          const uint32_t bbase = (kk < 4 ? b0 : b1) + koff;
+          const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + (koff >> 4);
           if (KV == IDX_KV_E4M3) {
-            umma_f8(d, umma_desc_sw128(a_base + koff), umma_desc_sw128(bbase), idesc, kk > 0);
+            umma_f8(d, adesc + (koff >> 4), bd, idesc, kk > 0);
           } else {
-            const uint32_t abase = a_base + (kk < 4 ? 0 : kTileKeys * 128) + koff;
-            umma_f16(d, umma_desc_sw128(abase), umma_desc_sw128(bbase), idesc, kk > 0);
+            umma_f16(d, adesc + (((kk < 4 ? 0u : static_cast<uint32_t>(kTileKeys) * 128u) + koff) >> 4), bd, idesc,
+                     kk > 0);
           }
         }
         umma_commit(&bars->empty[s]);
