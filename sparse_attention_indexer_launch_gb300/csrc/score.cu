@@ -331,10 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       }
       if (KV == IDX_KV_E4M3) {
         // lanes 0-15 copy page 0's 64 scales, lanes 16-31 page 1's, 16 bytes each
-        const int h = lane >> 4;
-        if (pages[h] >= 0)
-          cp_async16(sscale + ss * kTileKeys + lane * 4,
-                     a.k_scale + static_cast<int64_t>(pages[h]) * kPage + (lane & 15) * 4);
+        const int32_t pg = lane < 16 ? pages[0] : pages[1];
+        if (pg >= 0)
+          cp_async16(sscale + ss * kTileKeys + lane * 4, a.k_scale + static_cast<int64_t>(pg) * kPage + (lane & 15) * 4);
         cp_async_arrive_noinc(&bars->sfull[ss]);
       }
       last_k = k;
@@ -439,28 +438,40 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     bool ok = true;
 
     // Every row's histogram goes to global memory (12-bit counts, the 64-bin first
-    // digit, and the caller's copy of the latter when asked) and is cleared; all sixteen warps meet before and
-    // after, each flushing 16 of the 4 x 64 (row, first digit) blocks.
+    // digit, and the caller's copy of the latter when asked) and is cleared; all
+    // sixteen warps meet before and after.  The group's nrows x 64 (row, first digit)
+    // blocks of 64 bins are dealt round-robin to the warps, four at a time: the four
+    // shared-memory reads go out together, and a block with no count (most of them:
+    // a CTA's scores fill a few hundred of a row's 4096 bins) costs one vote.
     auto flush = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->hdone[0]);
       if (!mbar_wait(&bars->hdone[0], flushes & 1, limit, abort)) return false;
-      for (int b = ew * 16; b < ew * 16 + 16; ++b) {
-        const int row = b >> 6, d = b & 63;
-        if (row >= grp.nrows) break;       // uniform for the warp
-        uint32_t *h = shist + row * kHistWords;
-        const int64_t grow = grp.row0 + row;
-        const uint32_t wv = h[d * 32 + lane];
-        const uint32_t lo = wv & 0xFFFFu, hi = wv >> 16;
-        if (wv) {
-          h[d * 32 + lane] = 0u;
-          if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
-          if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
+      const int nblk = grp.nrows * 64;
+      for (int b0 = ew; b0 < nblk; b0 += 4 * kEpiWarps) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int b = b0 + i * kEpiWarps;
+          wv[i] = b < nblk ? shist[(b >> 6) * kHistWords + (b & 63) * 32 + lane] : 0u;
         }
-        const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
-        if (lane == 0 && dsum) {
-          atomicAdd(&ws.hist64[grow * 64 + d], dsum);
-          if (a.hist != nullptr) atomicAdd(&a.hist[grow * 64 + d], dsum);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (__ballot_sync(0xffffffffu, wv[i] != 0u) == 0u) continue;   // uniform for the warp
+          const int b = b0 + i * kEpiWarps;
+          const int row = b >> 6, d = b & 63;
+          const int64_t grow = grp.row0 + row;
+          const uint32_t lo = wv[i] & 0xFFFFu, hi = wv[i] >> 16;
+          if (wv[i]) {
+            shist[row * kHistWords + d * 32 + lane] = 0u;
+            if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
+            if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
+          }
+          const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
+          if (lane == 0) {
+            atomicAdd(&ws.hist64[grow * 64 + d], dsum);
+            if (a.hist != nullptr) atomicAdd(&a.hist[grow * 64 + d], dsum);
+          }
         }
       }
       __syncwarp();
