@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       mbar_init(&bars->empty[s], 1);
     }
     for (int s = 0; s < kScaleSlots; ++s) {
-      mbar_init(&bars->sfull[s], 32);          // one cp.async arrival per producer lane
+      mbar_init(&bars->sfull[s], 1);           // the producer's arrival; the copies complete by bytes
       mbar_init(&bars->sempty[s], kEpiWarps / 2);   // the eight warps of the tile's group
     }
     for (int s = 0; s < 2; ++s) {
@@ -317,6 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       }
       uint8_t *dst = sA + s * C::kStageBytes;
       if (lane == 0) {
+        if (KV == IDX_KV_E4M3) {
+          // the two pages' 64 scales each (256 bytes, one bulk copy per page)
+          mbar_arrive_expect_tx(&bars->sfull[ss], (pages[0] >= 0 ? 256u : 0u) + (pages[1] >= 0 ? 256u : 0u));
+          for (int h = 0; h < 2; ++h)
+            if (pages[h] >= 0)
+              bulk_load(sscale + ss * kTileKeys + h * kPage, a.k_scale + static_cast<int64_t>(pages[h]) * kPage, 256u,
+                        &bars->sfull[ss]);
+        }
         mbar_arrive_expect_tx(&bars->full[s], bytes);
         for (int h = 0; h < 2; ++h) {
           if (pages[h] < 0) continue;
@@ -328,13 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
                         policy);
           }
         }
-      }
-      if (KV == IDX_KV_E4M3) {
-        // lanes 0-15 copy page 0's 64 scales, lanes 16-31 page 1's, 16 bytes each
-        const int32_t pg = lane < 16 ? pages[0] : pages[1];
-        if (pg >= 0)
-          cp_async16(sscale + ss * kTileKeys + lane * 4, a.k_scale + static_cast<int64_t>(pg) * kPage + (lane & 15) * 4);
-        cp_async_arrive_noinc(&bars->sfull[ss]);
       }
       last_k = k;
     }
