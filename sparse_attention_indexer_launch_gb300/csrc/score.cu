@@ -298,7 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     };
     bool ok = true;
     int last_k = -1;
-    for (int64_t t = t0 + pp; t < t1; t += np) {
+    int s = pp;                 // this producer's stage of tile k and the phase it waits for
+    uint32_t ephase = 1u;
+    static_assert(C::kStages % kProducers == 0 || KV != IDX_KV_E4M3, "producers alternate stages");
+    for (int64_t t = t0 + pp; t < t1; t += np, s += np) {
+      if (s >= C::kStages) {
+        s -= C::kStages;
+        ephase ^= 1u;
+      }
       const int k = static_cast<int>(t - t0);
       if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
         const Group grp = gs[cur.g];
@@ -319,9 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       int32_t pages[2];
       pages[0] = __shfl_sync(0xffffffffu, blk_ids, (j & 15) * 2);
       pages[1] = __shfl_sync(0xffffffffu, blk_ids, (j & 15) * 2 + 1);
-      const int s = k % C::kStages;
       const int ss = k % kScaleSlots;
-      if (!warp_wait(&bars->empty[s], ((k / C::kStages) & 1) ^ 1) ||
+      if (!warp_wait(&bars->empty[s], ephase) ||
           (KV == IDX_KV_E4M3 && !warp_wait(&bars->sempty[ss], ((k / kScaleSlots) & 1) ^ 1))) {
         ok = false;
         break;
@@ -401,6 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       uint32_t idesc = 0;
       const uint32_t fmt = KV == IDX_KV_E4M3 ? 0u : 1u;
       const uint64_t bdesc0 = umma_desc_sw128(smem_u32(sB0)), bdesc1 = umma_desc_sw128(smem_u32(sB1));
+      // stage s of tile k and its phase, kept incrementally (no division per tile);
+      // stage s's A descriptor is stage 0's plus s stages of bytes / 16
+      const uint64_t adesc0 = umma_desc_sw128(smem_u32(sA));
+      int s = 0;
+      uint32_t sphase = 0;
       int k = 0;
       for (int64_t t = t0; t < t1; ++t, ++k) {
         cur.advance(static_cast<int>(t));
@@ -414,9 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           cur_g = cur.g;
           idesc = umma_idesc(fmt, 64u * gs[cur_g].nrows);
         }
-        const int s = k % C::kStages;
         const int acc = k & 1;
-        if (!mbar_wait(&bars->full[s], (k / C::kStages) & 1, limit, abort) ||
+        if (!mbar_wait(&bars->full[s], sphase, limit, abort) ||
             !mbar_wait(&bars->tempty[acc], ((k >> 1) & 1) ^ 1, limit, abort)) {
           set_abort(bars, ws.status);
           break;
@@ -425,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         const uint32_t d = tmem_base + acc * 256;
         // descriptors of the K steps: the base descriptor plus the step's byte offset / 16
         // (the start-address field holds address / 16; no carry out of it in 256 KB)
-        const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * C::kStageBytes));
+        const uint64_t adesc = adesc0 + static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = (kk & 3) * 32;
@@ -439,6 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         }
         umma_commit(&bars->empty[s]);
         if (!(a.stall_first_handoff && k == 0)) umma_commit(&bars->tfull[acc]);
+        if (++s == C::kStages) {
+          s = 0;
+          sphase ^= 1u;
+        }
       }
       // All MMAs issued by this thread complete before TMEM is released.
       umma_commit(&bars->drain);
