@@ -303,9 +303,18 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
         cm |= static_cast<uint32_t>(in && !w && xs[e] >= fc) << e;
       }
     };
-    // pass 1: count this thread's winners and candidates, remember the quads holding any
+    // pass 1: count this thread's winners and candidates, remember the quads holding any.
+    // Nearly every key is below both thresholds: a whole quad inside the slice with no
+    // key at or above the lower one (fc, or fw when fc takes nothing) is passed over
+    // after four compares.
+    const float flo = fc == fc ? fc : fw;
     uint32_t qmask = 0u, cw = 0u, cc = 0u;
     for (int i = 0; i < nq; ++i) {
+      const int q = i * kCollectThreads + tid;
+      if (4 * q + 3 < n) {
+        const float4 x = v4[q];
+        if (!(x.x >= flo || x.y >= flo || x.z >= flo || x.w >= flo)) continue;
+      }
       uint32_t wm, cm;
       masks(i, wm, cm);
       if (wm | cm) {
