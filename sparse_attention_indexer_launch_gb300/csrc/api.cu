@@ -4,7 +4,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <climits>
@@ -13,7 +12,6 @@
 #include "idx.h"
 #include "idx_device.cuh"
 #include "launch.h"
-#include "plan.cuh"
 
 namespace {
 
@@ -184,12 +182,6 @@ idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, 
   st = cuda_ok(idx::launch_prep(pa, s));
   if (st != IDX_OK) return st;
   idx::ScoreArgs sa{};
-  sa.row_req = p->row_req;
-  sa.row_bound = p->row_bound;
-  sa.R = p->R;
-  sa.Q = p->Q;
-  sa.bound_cap = std::min(static_cast<int64_t>(p->pt_stride) * IDX_PAGE, static_cast<int64_t>(p->max_bound));
-  sa.local_plan = p->R <= idx::kLocalPlanRows ? 1 : 0;
   sa.page_table = p->page_table;
   sa.k_scale = p->k_scale;
   sa.P = p->P;

@@ -20,11 +20,6 @@ struct PrepArgs {
 };
 
 struct ScoreArgs {
-  const int32_t *row_req;  // the plan's inputs: each CTA plans for itself when R <= kLocalPlanRows
-  const int32_t *row_bound;
-  int32_t R, Q;
-  int64_t bound_cap;       // min(pt_stride * page, max_bound)
-  int32_t local_plan;
   const int32_t *page_table;
   const float *k_scale;
   int64_t P;

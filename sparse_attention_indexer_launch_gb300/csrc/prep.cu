@@ -10,7 +10,6 @@
 
 #include "idx_device.cuh"
 #include "launch.h"
-#include "plan.cuh"
 
 namespace idx {
 namespace {
@@ -23,18 +22,120 @@ __device__ __forceinline__ uint32_t swz128(uint32_t n, uint32_t kbyte) {
   return n * 128u + ((((kbyte >> 4) ^ (n & 7u)) & 7u) << 4) + (kbyte & 15u);
 }
 
-// Publishes the plan (plan.cuh) for the scoring launch and the selection, clears
-// the status word and flags rows with a bad request or bound.
+template <typename T>
+__device__ T block_scan_incl(T v, T *tmp, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = is_max ? (n > v ? n : v) : v + n;
+  }
+  if (lane == 31) tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    T x = lane < (int)(blockDim.x >> 5) ? tmp[lane] : (is_max ? T(-2147483647 - 1) : T(0));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T n = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x = is_max ? (n > x ? n : x) : x + n;
+    }
+    tmp[lane] = x;
+  }
+  __syncthreads();
+  if (warp > 0) {
+    T p = tmp[warp - 1];
+    v = is_max ? (p > v ? p : v) : v + p;
+  }
+  __syncthreads();
+  return v;
+}
+
+// Row groups by the join rule of the sglang PR 48224 page (section Reviewer
+// notes, "The join rule"): row r joins row r-1's group when both belong to the
+// same request and bound[r] == bound[r-1] + 1, and a group holds at most four
+// rows (section Modifications, commit 1: rows of one request read and convert
+// each key once for all of them).  Every other row starts a new group.
 __device__ void plan_block(const PrepArgs &a) {
+  __shared__ int32_t tmp[32];
+  __shared__ int32_t carry_run, carry_group, carry_tiles;
+  const int R = a.R;
   const Workspace &ws = a.ws;
   const int64_t bound_cap = min(static_cast<int64_t>(a.pt_stride) * kPage, static_cast<int64_t>(a.max_bound));
-  if (threadIdx.x == 0) *ws.status = 0u;
-  __syncthreads();
-  const PlanResult pr = plan_rows(a.row_req, a.row_bound, a.R, a.Q, bound_cap, ws.groups, ws.bound_eff);
   if (threadIdx.x == 0) {
-    if (pr.bad) atomicOr(ws.status, kStatusBadBound);
-    ws.plan->num_groups = pr.num_groups;
-    ws.plan->total_tiles = pr.total_tiles;
+    carry_run = 0;
+    carry_group = 0;
+    carry_tiles = 0;
+    *ws.status = 0u;
+  }
+  __syncthreads();
+  bool bad = false;
+  // Pass 1: effective bounds, group starts, group records (req, row0).
+  for (int base = 0; base < R; base += kPrepThreads) {
+    const int r = base + threadIdx.x;
+    bool join = false, gstart = false;
+    int32_t rs = -1;
+    if (r < R) {
+      const int32_t req = a.row_req[r];
+      const int32_t braw = a.row_bound[r];
+      const bool ok = req >= 0 && req < a.Q && braw >= 0 && braw <= bound_cap;
+      if (!ok) bad = true;
+      ws.bound_eff[r] = (req >= 0 && req < a.Q) ? static_cast<int32_t>(max(int64_t{0}, min(static_cast<int64_t>(braw), bound_cap))) : 0;
+      if (ok && r > 0) {
+        const int32_t reqp = a.row_req[r - 1];
+        const int32_t bp = a.row_bound[r - 1];
+        join = reqp == req && bp >= 0 && braw == bp + 1;
+      }
+      if (!join) rs = r;
+    }
+    // run start: the last non-joining row at or before r
+    rs = block_scan_incl<int32_t>(rs, tmp, true);
+    if (rs < 0) rs = carry_run;
+    gstart = (r < R) && (!join || ((r - rs) % kMaxGroupRows) == 0);
+    int32_t gi = block_scan_incl<int32_t>(gstart ? 1 : 0, tmp, false) + carry_group - 1;
+    if (gstart) {
+      const int32_t req = a.row_req[r];
+      Group g;
+      g.req = (req >= 0 && req < a.Q) ? req : -1;
+      g.row0 = r;
+      g.nrows = 0;
+      g.L = 0;
+      g.tile_begin = 0;
+      g.pad[0] = g.pad[1] = g.pad[2] = 0;
+      ws.groups[gi] = g;
+    }
+    __syncthreads();
+    if (threadIdx.x == kPrepThreads - 1) {
+      carry_run = rs;
+      carry_group = gi + 1;
+    }
+    __syncthreads();
+  }
+  const int G = carry_group;
+  __syncthreads();
+  // Pass 2: rows per group, keys read (largest bound), tiles and their prefix.
+  for (int base = 0; base < G; base += kPrepThreads) {
+    const int g = base + threadIdx.x;
+    int32_t tiles = 0;
+    if (g < G) {
+      const int32_t r0 = ws.groups[g].row0;
+      const int32_t r1 = (g + 1 < G) ? ws.groups[g + 1].row0 : R;
+      int32_t L = 0;
+      for (int r = r0; r < r1; ++r) L = max(L, ws.bound_eff[r]);
+      if (ws.groups[g].req < 0) L = 0;
+      ws.groups[g].nrows = r1 - r0;
+      ws.groups[g].L = L;
+      tiles = (L + kTileKeys - 1) / kTileKeys;
+    }
+    int32_t incl = block_scan_incl<int32_t>(tiles, tmp, false);
+    if (g < G) ws.groups[g].tile_begin = carry_tiles + incl - tiles;
+    __syncthreads();
+    if (threadIdx.x == kPrepThreads - 1) carry_tiles += incl;
+    __syncthreads();
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(ws.status, kStatusBadBound);
+  if (threadIdx.x == 0) {
+    ws.plan->num_groups = G;
+    ws.plan->total_tiles = carry_tiles;
   }
 }
 

@@ -33,7 +33,6 @@
 // bf16 cache: keys and query are bf16, kind::f16, K = 128.
 #include "idx_device.cuh"
 #include "launch.h"
-#include "plan.cuh"
 
 namespace idx {
 namespace {
@@ -78,8 +77,7 @@ struct Smem {
   static constexpr int kHist = kA + Cfg<KV>::kStages * Cfg<KV>::kStageBytes;
   static constexpr int kScales = kHist + kMaxGroupRows * kHistWords * 4;
   static constexpr int kW = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
-  static constexpr int kGroups = kW + kEpiWarps * 2 * kHeads * 4;
-  static constexpr int kBars = kGroups + kLocalPlanRows * static_cast<int>(sizeof(Group));
+  static constexpr int kBars = kW + kEpiWarps * 2 * kHeads * 4;
   static constexpr int kBytes = kBars + static_cast<int>(sizeof(Barriers));
   static constexpr int kDynamic = kBytes + 1024;  // alignment slack
 };
@@ -114,15 +112,8 @@ struct GroupCursor {
   }
 };
 
-// The prep launch clears the status word, so a flag raised while it may still be
-// running waits for it first.
-__device__ __forceinline__ void score_flag(uint32_t *status, uint32_t bits) {
-  grid_dependency_wait();
-  flag_status(status, bits);
-}
-
 __device__ __forceinline__ void set_abort(Barriers *bars, uint32_t *status) {
-  score_flag(status, kStatusTimeout);
+  flag_status(status, kStatusTimeout);
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
@@ -176,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   uint32_t *shist = reinterpret_cast<uint32_t *>(smem + S::kHist);   // [row][2048] packed 16-bit counts
   float *sscale = reinterpret_cast<float *>(smem + S::kScales);     // [slot][128]
   float *sw = reinterpret_cast<float *>(smem + S::kW);              // [epilogue warp][64]
-  Group *sgroups = reinterpret_cast<Group *>(smem + S::kGroups);   // the CTA's own plan
   Barriers *bars = reinterpret_cast<Barriers *>(smem + S::kBars);
 
   const int warp = threadIdx.x >> 5;
@@ -214,27 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dependency_trigger();
-  // The plan.  With few enough rows every CTA computes it from the launch's inputs,
-  // so that its key loads start while the prep launch still runs; the roles wait
-  // for that launch only where they read what it writes (the query operands, the
-  // weights and bounds, the cleared histograms and status).  Else the plan is the
-  // prep launch's.
-  const Group *gs;
-  int total_tiles, num_groups;
-  if (a.local_plan) {
-    const PlanResult pr = plan_rows(a.row_req, a.row_bound, a.R, a.Q, a.bound_cap, sgroups, nullptr);
-    gs = sgroups;
-    total_tiles = pr.total_tiles;
-    num_groups = pr.num_groups;
-  } else {
-    grid_dependency_wait();
-    gs = ws.groups;
-    total_tiles = ws.plan->total_tiles;
-    num_groups = ws.plan->num_groups;
-  }
+  grid_dependency_wait();   // the plan and the query operands come from the prep launch
+  const int total_tiles = ws.plan->total_tiles;
+  const int num_groups = ws.plan->num_groups;
   const int64_t t0 = static_cast<int64_t>(total_tiles) * blockIdx.x / gridDim.x;
   const int64_t t1 = static_cast<int64_t>(total_tiles) * (blockIdx.x + 1) / gridDim.x;
+  grid_dependency_trigger();
   if (t0 >= t1) {  // uniform for the CTA: no tiles, give the TMEM back
     if (warp == 1) tmem_dealloc(bars->tmem_base, kTmemCols);
     return;
@@ -256,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     const int np = KV == IDX_KV_E4M3 ? kProducers : 1;
     const uint64_t policy = l2_evict_first_policy();
     GroupCursor cur;
-    cur.seek(gs, num_groups, static_cast<int>(t0));
+    cur.seek(ws.groups, num_groups, static_cast<int>(t0));
     int cur_g = -1, req = 0, L = 0, tile_begin = 0;
     int32_t blk_ids = -2, nxt_ids = -2;   // this lane's page id in the current / next block
     int blk = -1;                          // current block of 16 tiles within the group
@@ -277,14 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     int bg = cur.g;                             // next group to consider (seek lands on a group with tiles)
     auto load_b_upto = [&](int64_t upto) -> bool {
       while (bg < num_groups) {
-        const int begin = gs[bg].tile_begin;
+        const int begin = ws.groups[bg].tile_begin;
         if (begin > upto || begin >= t1) break;
-        const int end = bg + 1 < num_groups ? gs[bg + 1].tile_begin : total_tiles;
+        const int end = bg + 1 < num_groups ? ws.groups[bg + 1].tile_begin : total_tiles;
         if (end > begin) {
           if (nb > 0 && !warp_wait(&bars->bfree, (nb - 1) & 1)) return false;
           if (lane == 0) {
-            grid_dependency_wait();   // the query operands come from the prep launch
-            const Group grp = gs[bg];
+            const Group grp = ws.groups[bg];
             const uint32_t bytes = grp.nrows * kRowOperandBytes;
             mbar_arrive_expect_tx(&bars->bfull, 2 * bytes);
             bulk_load(sB0, ws.qop0 + static_cast<int64_t>(grp.row0) * kRowOperandBytes, bytes, &bars->bfull);
@@ -307,8 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         ephase ^= 1u;
       }
       const int k = static_cast<int>(t - t0);
+      if (pp == 0 && !load_b_upto(t)) {
+        ok = false;
+        break;
+      }
       if (cur.advance(static_cast<int>(t)) || cur_g < 0) {
-        const Group grp = gs[cur.g];
+        const Group grp = ws.groups[cur.g];
         cur_g = cur.g;
         req = grp.req;
         L = grp.L;
@@ -340,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           bytes += C::kPageBytes;
         } else {
           pages[h] = -1;
-          if (lane == 0) score_flag(ws.status, kStatusBadPage);
+          if (lane == 0) flag_status(ws.status, kStatusBadPage);
         }
       }
       uint8_t *dst = sA + s * C::kStageBytes;
@@ -366,12 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         }
       }
       last_k = k;
-      // the query operands of the groups up to this tile, after the tile's own
-      // loads (the first waits for the prep launch)
-      if (pp == 0 && !load_b_upto(t)) {
-        ok = false;
-        break;
-      }
     }
     if (ok && pp == 0) ok = load_b_upto(t1 - 1);   // groups whose tiles all fell to the other producer
     if (!ok && lane == 0) set_abort(bars, ws.status);
@@ -387,22 +359,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     for (int s = 0; s < C::kStages; ++s) {
       const int lu = last_use(s, C::kStages);
       if (lu >= 0 && !mbar_wait(&bars->full[s], (lu / C::kStages) & 1, limit, &never) && lane == 0)
-        score_flag(ws.status, kStatusTimeout);
+        flag_status(ws.status, kStatusTimeout);
     }
     if (KV == IDX_KV_E4M3) {
       for (int s = 0; s < kScaleSlots; ++s) {
         const int lu = last_use(s, kScaleSlots);
         if (lu >= 0 && !mbar_wait(&bars->sfull[s], (lu / kScaleSlots) & 1, limit, &never) && lane == 0)
-          score_flag(ws.status, kStatusTimeout);
+          flag_status(ws.status, kStatusTimeout);
       }
     }
     if (pp == 0 && nb > 0 && !mbar_wait(&bars->bfull, (nb - 1) & 1, limit, &never) && lane == 0)
-      score_flag(ws.status, kStatusTimeout);
+      flag_status(ws.status, kStatusTimeout);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       GroupCursor cur;
-      cur.seek(gs, num_groups, static_cast<int>(t0));
+      cur.seek(ws.groups, num_groups, static_cast<int>(t0));
       int cur_g = -1, nswitch = 0;
       uint32_t idesc = 0;
       const uint32_t fmt = KV == IDX_KV_E4M3 ? 0u : 1u;
@@ -423,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           }
           ++nswitch;
           cur_g = cur.g;
-          idesc = umma_idesc(fmt, 64u * gs[cur_g].nrows);
+          idesc = umma_idesc(fmt, 64u * ws.groups[cur_g].nrows);
         }
         const int acc = k & 1;
         if (!mbar_wait(&bars->full[s], sphase, limit, abort) ||
@@ -457,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       // All MMAs issued by this thread complete before TMEM is released.
       umma_commit(&bars->drain);
       int never = 0;
-      if (!mbar_wait(&bars->drain, 0, limit, &never)) score_flag(ws.status, kStatusTimeout);
+      if (!mbar_wait(&bars->drain, 0, limit, &never)) flag_status(ws.status, kStatusTimeout);
     }
   } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------------ epilogue
@@ -470,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     const int r0 = (slot >> 1) * 2;          // first of this warp's two group rows
     float *myw = sw + ew * 2 * kHeads;       // the two rows' weights
     GroupCursor cur;
-    cur.seek(gs, num_groups, static_cast<int>(t0));
+    cur.seek(ws.groups, num_groups, static_cast<int>(t0));
     int cur_g = -1;
     Group grp;
     grp.nrows = 0;
@@ -528,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // and every kFlushTiles tiles within a group; 16-bit counters) are defined on
     // the CTA's tile sequence and every warp takes each of them, in order.
     auto load_group = [&]() {
-      grp = gs[cur.g];
+      grp = ws.groups[cur.g];
       __syncwarp();
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -559,7 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       if (upto > done) done = upto;
       return true;
     };
-    grid_dependency_wait();   // weights, bounds and cleared histograms come from the prep launch
     load_group();
     cur_g = cur.g;
 
