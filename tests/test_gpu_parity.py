@@ -34,7 +34,7 @@ SMALL = [
     ("rows_out_of_order", [700, 900], [3, 2], "e4m3", {"row_order": [3, 0, 4, 1, 2]}),
     ("around_k", [2047, 2048, 2049, 4096], [1, 1, 1, 1], "e4m3", {}),
     ("around_k_bf16", [2047, 2048, 2049, 4100], [2, 1, 3, 1], "bf16", {}),
-    # more rows than a scoring CTA plans for itself: the scan takes the prep launch's plan
+    # 600 rows in 150 requests: the plan's passes and group records span several blocks of rows
     ("many_rows", [(i * 97) % 2900 + 64 for i in range(150)], [4] * 150, "e4m3", {}),
 ]
 
