@@ -58,6 +58,10 @@ __device__ T block_scan_incl(T v, T *tmp, bool is_max) {
 __device__ void plan_block(const PrepArgs &a) {
   __shared__ int32_t tmp[32];
   __shared__ int32_t carry_run, carry_group, carry_tiles;
+  // With at most one block of rows the whole plan stays in shared memory until it
+  // is written out once: each group's first row and request, each row's bound.
+  __shared__ int32_t s_row0[kPrepThreads], s_req[kPrepThreads], s_eff[kPrepThreads];
+  const bool one_pass = a.R <= kPrepThreads;
   const int R = a.R;
   const Workspace &ws = a.ws;
   const int64_t bound_cap = min(static_cast<int64_t>(a.pt_stride) * kPage, static_cast<int64_t>(a.max_bound));
@@ -79,7 +83,10 @@ __device__ void plan_block(const PrepArgs &a) {
       const int32_t braw = a.row_bound[r];
       const bool ok = req >= 0 && req < a.Q && braw >= 0 && braw <= bound_cap;
       if (!ok) bad = true;
-      ws.bound_eff[r] = (req >= 0 && req < a.Q) ? static_cast<int32_t>(max(int64_t{0}, min(static_cast<int64_t>(braw), bound_cap))) : 0;
+      const int32_t eff =
+          (req >= 0 && req < a.Q) ? static_cast<int32_t>(max(int64_t{0}, min(static_cast<int64_t>(braw), bound_cap))) : 0;
+      ws.bound_eff[r] = eff;
+      if (one_pass) s_eff[r] = eff;
       if (ok && r > 0) {
         const int32_t reqp = a.row_req[r - 1];
         const int32_t bp = a.row_bound[r - 1];
@@ -94,14 +101,19 @@ __device__ void plan_block(const PrepArgs &a) {
     int32_t gi = block_scan_incl<int32_t>(gstart ? 1 : 0, tmp, false) + carry_group - 1;
     if (gstart) {
       const int32_t req = a.row_req[r];
-      Group g;
-      g.req = (req >= 0 && req < a.Q) ? req : -1;
-      g.row0 = r;
-      g.nrows = 0;
-      g.L = 0;
-      g.tile_begin = 0;
-      g.pad[0] = g.pad[1] = g.pad[2] = 0;
-      ws.groups[gi] = g;
+      if (one_pass) {
+        s_row0[gi] = r;
+        s_req[gi] = (req >= 0 && req < a.Q) ? req : -1;
+      } else {
+        Group g;
+        g.req = (req >= 0 && req < a.Q) ? req : -1;
+        g.row0 = r;
+        g.nrows = 0;
+        g.L = 0;
+        g.tile_begin = 0;
+        g.pad[0] = g.pad[1] = g.pad[2] = 0;
+        ws.groups[gi] = g;
+      }
     }
     __syncthreads();
     if (threadIdx.x == kPrepThreads - 1) {
@@ -113,7 +125,31 @@ __device__ void plan_block(const PrepArgs &a) {
   const int G = carry_group;
   __syncthreads();
   // Pass 2: rows per group, keys read (largest bound), tiles and their prefix.
-  for (int base = 0; base < G; base += kPrepThreads) {
+  if (one_pass) {   // G <= R <= kPrepThreads: one group per thread, from shared memory
+    const int g = threadIdx.x;
+    int32_t tiles = 0, r0 = 0, r1 = 0, L = 0;
+    if (g < G) {
+      r0 = s_row0[g];
+      r1 = (g + 1 < G) ? s_row0[g + 1] : R;
+      for (int r = r0; r < r1; ++r) L = max(L, s_eff[r]);
+      if (s_req[g] < 0) L = 0;
+      tiles = (L + kTileKeys - 1) / kTileKeys;
+    }
+    const int32_t incl = block_scan_incl<int32_t>(tiles, tmp, false);
+    if (g < G) {
+      Group gr;
+      gr.req = s_req[g];
+      gr.row0 = r0;
+      gr.nrows = r1 - r0;
+      gr.L = L;
+      gr.tile_begin = incl - tiles;
+      gr.pad[0] = gr.pad[1] = gr.pad[2] = 0;
+      ws.groups[g] = gr;
+    }
+    if (threadIdx.x == kPrepThreads - 1) carry_tiles = incl;
+    __syncthreads();
+  }
+  for (int base = 0; !one_pass && base < G; base += kPrepThreads) {
     const int g = base + threadIdx.x;
     int32_t tiles = 0;
     if (g < G) {

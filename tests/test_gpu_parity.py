@@ -36,6 +36,9 @@ SMALL = [
     ("around_k_bf16", [2047, 2048, 2049, 4100], [2, 1, 3, 1], "bf16", {}),
     # 600 rows in 150 requests: the plan's passes and group records span several blocks of rows
     ("many_rows", [(i * 97) % 2900 + 64 for i in range(150)], [4] * 150, "e4m3", {}),
+    # more rows than one block of the planning pass: the plan's group records go
+    # through global memory between its two passes
+    ("rows_over_1024", [(i * 53) % 600 + 1 for i in range(280)], [4] * 280, "e4m3", {}),
 ]
 
 
