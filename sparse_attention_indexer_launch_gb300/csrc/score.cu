@@ -19,7 +19,7 @@
 //   warp 0      producer (with warp 18 for an E4M3 cache: even / odd tiles):
 //               page ids (32 per lane load, a block ahead), TMA of the
 //               key pages into an smem ring, the keys' scales into a second ring
-//               (cp.async by the warp's lanes), and the group's query operand
+//               (two 256-byte bulk copies per tile), and the group's query operand
 //               (bulk copy) on group changes;
 //   warp 1      MMA issuer (one thread) and TMEM owner; two accumulators in TMEM,
 //               so the MMA of tile k+1 runs while tile k's epilogue reads;
@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // warp kProducer2Warp for the odd ones (their key stages and scale slots are
     // disjoint: both ring lengths are even); bf16: warp 0 alone.  In each, the whole
     // warp runs the loop: lanes hold the page ids of the current and next block of
-    // 16 tiles (32 pages, one lane each) and copy the tile's 128 key scales (16 bytes
-    // per lane); lane 0 issues the key pages' TMA.  Warp 0 also loads the query
+    // 16 tiles (32 pages, one lane each); lane 0 issues the key pages' TMA and the
+    // bulk copies of their 128 key scales.  Warp 0 also loads the query
     // operand of every group of the range, in order.
     const int pp = warp == 0 ? 0 : 1;           // this producer's tile parity
     const int np = KV == IDX_KV_E4M3 ? kProducers : 1;
