@@ -505,6 +505,12 @@ def main():
     else:
         achieved, peak, unit = flops / score_s / 1e12, fp8_tf, "TFLOP/s"
     traffic = profile_traffic(os.path.join(ROOT, "sparse_attention_indexer_launch_gb300", "csrc", "score.cu"))
+    # The epilogue's ALU term: 128 lane operations per (key, row) (64 max + 64 FMA)
+    # over every SM's 128 FP32 lanes at the sampled SM clock.
+    clk = clocks.summary(t_start, t_end)
+    sm_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 0.0
+    n_sms = torch.cuda.get_device_properties(local).multi_processor_count
+    alu_floor_us = prob.key_rows * 128 / (n_sms * 128 * sm_mhz * 1e6) * 1e6 if sm_mhz else None
 
     if rank == 0:
         line = {
@@ -534,8 +540,9 @@ def main():
                          "launch_roofline_us": t_roof * 1e6,
                          "launch_frac_of_roofline": t_roof / (ms * 1e-3),
                          "tensor_frac_fp8": flops / score_s / 1e12 / fp8_tf,
-                         "tensor_frac_bf16_precision_matched": flops / score_s / 1e12 / bf16_tf},
-            "clocks": clocks.summary(t_start, t_end),
+                         "tensor_frac_bf16_precision_matched": flops / score_s / 1e12 / bf16_tf,
+                         "alu_epilogue_floor_us": alu_floor_us},
+            "clocks": clk,
             "gpu_launches": KERNELS_PER_LAUNCH * args.steps,
             "wall_s_timed_region": t_wall,
         }
