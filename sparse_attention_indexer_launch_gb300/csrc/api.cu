@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <climits>
@@ -108,22 +109,22 @@ idx_status check_problem(const idx_problem *p) {
 }
 
 // ---------------------------------------------------------------------------- device info
-int g_num_sms[128];
+std::atomic<int> g_num_sms[128];   // filled on first use per device (concurrent callers store the same value)
 
 idx_status device_sms(int *out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ECUDA;
   if (dev < 0 || dev >= 128) return IDX_EUNSUPPORTED;
-  if (g_num_sms[dev] == 0) {
+  if (g_num_sms[dev].load(std::memory_order_relaxed) == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IDX_ECUDA;
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (major != 10 || minor != 3) return IDX_EUNSUPPORTED;  // built for sm_103a only
-    g_num_sms[dev] = n;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
   }
-  *out = g_num_sms[dev];
+  *out = g_num_sms[dev].load(std::memory_order_relaxed);
   return IDX_OK;
 }
 
