@@ -4,9 +4,26 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "idx_device.cuh"
 
 namespace idx {
+
+// Runs setup() once per device (the current one) and remembers that it succeeded;
+// safe to call from several host threads.  `done` is a caller-owned flag table.
+template <typename F>
+inline cudaError_t once_per_device(std::mutex &mu, bool (&done)[128], F setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return cudaSuccess;
+  e = setup();
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
 
 struct PrepArgs {
   const void *q;

@@ -610,13 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 
 template <int KV>
 cudaError_t launch_kv(const CUtensorMap &kmap, const ScoreArgs &a, int num_ctas, cudaStream_t stream) {
-  static bool configured = false;
+  static std::mutex mu;
+  static bool done[128] = {};
   constexpr int bytes = Smem<KV>::kDynamic;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(score_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = once_per_device(mu, done, [] {
+    return cudaFuncSetAttribute(score_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
   cfg.blockDim = dim3(kThreads);

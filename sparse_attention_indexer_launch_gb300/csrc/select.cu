@@ -834,14 +834,15 @@ int collect_slice(const SelectArgs &a) {
 }
 
 cudaError_t launch_collect(const SelectArgs &a_in, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmemAlloc);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCollectSmemAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::mutex mu;
+  static bool done[128] = {};
+  const cudaError_t es = once_per_device(mu, done, [] {
+    const cudaError_t e1 =
+        cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishSmemAlloc);
+    if (e1 != cudaSuccess) return e1;
+    return cudaFuncSetAttribute(collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCollectSmemAlloc);
+  });
+  if (es != cudaSuccess) return es;
   SelectArgs a = a_in;
   a.slice = collect_slice(a);
   cudaLaunchAttribute attr[1];
