@@ -29,6 +29,12 @@
  *     with idx_last_device_status().
  *   - Key positions are logical positions within the row's request: position t
  *     lives in physical page page_table[req * pt_stride + t / 64], slot t % 64.
+ *   - Host threads: any call may be made from several host threads at once, on
+ *     the same or different devices, as long as concurrent calls use different
+ *     workspaces (the library's one-time per-device setup is serialised inside
+ *     it).  idx_topk_noalloc is the exception: its scratch is one per device.
+ *     idx_debug_set and idx_profile_events change process-wide state that the
+ *     next call from any thread picks up.
  */
 #ifndef IDX_H
 #define IDX_H
