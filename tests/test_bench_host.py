@@ -39,3 +39,18 @@ def test_traffic_follows_the_kernel_source(tmp_path):
     other = tmp_path / "score.cu"
     other.write_bytes(open(SCORE_SRC, "rb").read() + b"\n// changed\n")
     assert bench.profile_traffic(str(other)) is None
+
+
+def test_cpu_baseline_sample_is_bounded_and_described():
+    import oracle
+    import workloads
+    prob = workloads.make_config(0)           # one row of 4,096 keys: the oracle takes milliseconds
+    orc = oracle.default()
+    r = bench.cpu_baseline(prob, orc, budget_s=0.3)
+    assert r["kind"] == "oracle" and r["unit"] == "key·rows/s"
+    assert r["value"] > 0 and r["cores"] >= 1
+    assert r["seconds"] < 2.0                 # about the budget, never far past it
+    assert "pass(es) over the whole workload" in r["sample"]   # the workload fits: whole passes
+    # a budget far below one pass cuts the rows instead of repeating them
+    cut = bench.cpu_baseline(prob, orc, budget_s=1e-7, rate_hint=r["rate"])
+    assert "of 1 rows" in cut["sample"] and cut["value"] > 0
