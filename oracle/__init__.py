@@ -73,6 +73,8 @@ def _bind(path: str):
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_quantize_key.argtypes = [p, p, p]
     lib.oracle_quantize_key.restype = None
+    lib.oracle_patch_new_keys.argtypes = [p, p, p, i32, p, i64, i32, p, p, i32, i64]
+    lib.oracle_patch_new_keys.restype = i32
     lib.oracle_top1.argtypes = [p, i64, i32, i64, p, p]
     lib.oracle_top1.restype = None
     lib.oracle_num_threads.argtypes = []
@@ -182,23 +184,21 @@ class Oracle:
     def patch_new_keys(self, prob, k_new_bits):
         """A copy of prob with every row's new key written at its position
         row_bound - 1 (rows with bound 0 write nothing): E4M3 codes and scale, or
-        the bf16 values for a bf16 cache."""
+        the bf16 values for a bf16 cache (oracle_patch_new_keys)."""
         import copy
         out = copy.copy(prob)
-        out.k_cache = prob.k_cache.copy()
-        out.k_scale = None if prob.k_scale is None else prob.k_scale.copy()
-        for r in range(prob.R):
-            b = int(prob.row_bound[r])
-            if b <= 0:
-                continue
-            t = b - 1
-            page = int(prob.page_table[prob.row_req[r], t // 64])
-            if prob.kv_dtype == "e4m3":
-                codes, sc = self.quantize_key(k_new_bits[r])
-                out.k_cache[page, t % 64] = codes
-                out.k_scale[page, t % 64] = sc
-            else:
-                out.k_cache[page, t % 64] = k_new_bits[r]
+        kv, kc, ks = _kv(prob)
+        out.k_cache = kc.copy()
+        out.k_scale = None if ks is None else ks.copy()
+        kn = _c(k_new_bits, np.uint16)
+        rr = _c(prob.row_req, np.int32)
+        rb = _c(prob.row_bound, np.int32)
+        pt = _c(prob.page_table, np.int32)
+        rc = self.lib.oracle_patch_new_keys(_ptr(kn), _ptr(rr), _ptr(rb), rb.shape[0], _ptr(pt), pt.shape[1],
+                                            pt.shape[0], _ptr(out.k_cache), _ptr(out.k_scale), kv,
+                                            out.k_cache.shape[0])
+        if rc != 0:
+            raise ValueError("oracle_patch_new_keys: request, bound or page id out of range")
         return out
 
     def top1(self, logits_f32):

@@ -87,8 +87,8 @@ uint8_t oracle_e4m3_encode(float x) {
 }
 
 /* The new key of a decode row, as the launch writes it into the paged cache (the
- * later commit "New keys, as #74 has them" on the page: a key this launch writes
- * is scored for every row of its request).  E4M3 cache: scale = amax / 448 in fp32
+ * page's Reviewer notes, "New keys": a key that the launch writes is scored for
+ * every row of its request).  E4M3 cache: scale = amax / 448 in fp32
  * (1 for a zero key), each value x / scale in fp32, clamped to +-448, encoded to
  * the nearest E4M3 code.  bf16 cache: the values as given.  key_bf16 [128]. */
 void oracle_quantize_key(const uint16_t *key_bf16, uint8_t *codes, float *scale) {
@@ -100,6 +100,54 @@ void oracle_quantize_key(const uint16_t *key_bf16, uint8_t *codes, float *scale)
     const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
     for (int i = 0; i < ORACLE_DIM; ++i) codes[i] = oracle_e4m3_encode((float)oracle_bf16_to_double(key_bf16[i]) / sc);
     *scale = sc;
+}
+
+/* Where row r's new key goes: logical position t = row_bound[r] - 1 of its
+ * request, i.e. page id *page at slot *slot.  Returns 0 for a row with bound 0
+ * (it adds no key), 1 otherwise. */
+static int new_key_target(const int32_t *row_req, const int32_t *row_bound, const int32_t *page_table,
+                          int64_t pt_stride, int r, int64_t *page, int64_t *slot) {
+    if (row_bound[r] == 0) return 0;
+    const int64_t t = (int64_t)row_bound[r] - 1;
+    *page = page_table[(int64_t)row_req[r] * pt_stride + t / ORACLE_PAGE];
+    *slot = t % ORACLE_PAGE;
+    return 1;
+}
+
+/* Writes every row's new key into the paged cache (the page's Reviewer notes,
+ * "New keys": the key a decode row adds sits at the row's last visible position,
+ * bound - 1, and is scored by every row of its request whose bound covers it).
+ * Row r's key goes to logical position t = row_bound[r] - 1 of request
+ * row_req[r]: physical page page_table[req * pt_stride + t / 64], slot t % 64.
+ * Rows with bound 0 add no key.  E4M3 cache (kv_dtype 0): oracle_quantize_key's
+ * codes and scale; bf16 cache (kv_dtype 1): the bf16 values as given.
+ *   k_new [R][128] bf16 bit patterns; k_cache / k_scale are written in place.
+ * Returns 0, or -1 (nothing written) if a row's request, bound or page id is out
+ * of range. */
+int oracle_patch_new_keys(const uint16_t *k_new, const int32_t *row_req, const int32_t *row_bound, int R,
+                          const int32_t *page_table, int64_t pt_stride, int Q, void *k_cache, float *k_scale,
+                          int kv_dtype, int64_t P) {
+    int64_t page, slot;
+    for (int r = 0; r < R; ++r) {
+        if (row_req[r] < 0 || row_req[r] >= Q || row_bound[r] < 0 ||
+            (int64_t)row_bound[r] > pt_stride * ORACLE_PAGE)
+            return -1;
+        if (new_key_target(row_req, row_bound, page_table, pt_stride, r, &page, &slot) &&
+            (page < 0 || page >= P))
+            return -1;
+    }
+    for (int r = 0; r < R; ++r) {
+        if (!new_key_target(row_req, row_bound, page_table, pt_stride, r, &page, &slot)) continue;
+        const uint16_t *key = k_new + (int64_t)r * ORACLE_DIM;
+        if (kv_dtype == 0) {
+            oracle_quantize_key(key, (uint8_t *)k_cache + (page * ORACLE_PAGE + slot) * ORACLE_DIM,
+                                &k_scale[page * ORACLE_PAGE + slot]);
+        } else {
+            memcpy((uint16_t *)k_cache + (page * ORACLE_PAGE + slot) * ORACLE_DIM, key,
+                   ORACLE_DIM * sizeof(uint16_t));
+        }
+    }
+    return 0;
 }
 
 /* bfloat16: the upper 16 bits of an IEEE binary32. */

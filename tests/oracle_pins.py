@@ -436,20 +436,39 @@ def pin_quantize_key(orc):
 
 
 def pin_patch_position(orc):
-    prob = workloads.build("patch", [300, 130], [2, 1], "e4m3", seed=33)
+    """New keys land at hand-worked cache cells.  Page table [[5, 2, 7], [0, 3, 1]]
+    over 8 pages; a row's key goes to logical position bound - 1:
+      request 0, bound 70  -> t = 69:  page index 1 -> page 2, slot 5
+      request 0, bound 129 -> t = 128: page index 2 -> page 7, slot 0
+      request 0, bound 1   -> t = 0:   page index 0 -> page 5, slot 0
+      request 1, bound 64  -> t = 63:  page index 0 -> page 0, slot 63
+      request 0, bound 0   -> no key
+    Every other cell keeps its bytes (and scale)."""
+    expect = {(2, 5): 0, (7, 0): 1, (5, 0): 2, (0, 63): 3}      # cell -> row whose key it holds
     rng = np.random.default_rng(34)
-    k_new = torch.from_numpy(rng.standard_normal((prob.R, 128)).astype(np.float32)).to(torch.bfloat16) \
-        .view(torch.int16).numpy().view(np.uint16)
-    out = orc.patch_new_keys(prob, k_new)
-    changed = np.argwhere((out.k_cache != prob.k_cache).any(axis=2))
-    expect = set()
-    for r in range(prob.R):
-        t = int(prob.row_bound[r]) - 1
-        page = int(prob.page_table[prob.row_req[r], t // 64])
-        expect.add((page, t % 64))
-        codes, sc = orc.quantize_key(k_new[r])
-        assert np.array_equal(out.k_cache[page, t % 64], codes) and out.k_scale[page, t % 64] == sc
-    assert set(map(tuple, changed.tolist())) <= expect
+    for kv in ("e4m3", "bf16"):
+        R, P = 5, 8
+        k_new = torch.from_numpy((rng.standard_normal((R, 128)) + 0.5).astype(np.float32)).to(torch.bfloat16) \
+            .view(torch.int16).numpy().view(np.uint16)
+        prob = workloads.Problem(
+            name="patch_literal", q=np.zeros((R, 64, 128), np.uint16), w=np.zeros((R, 64), np.float32),
+            k_cache=np.zeros((P, 64, 128), np.uint8 if kv == "e4m3" else np.uint16),
+            k_scale=np.full((P, 64), 0.5, np.float32) if kv == "e4m3" else None,
+            page_table=np.array([[5, 2, 7], [0, 3, 1]], np.int32),
+            row_req=np.array([0, 0, 0, 1, 0], np.int32), row_bound=np.array([70, 129, 1, 64, 0], np.int32),
+            kv_dtype=kv)
+        out = orc.patch_new_keys(prob, k_new)
+        changed = {tuple(c) for c in np.argwhere((out.k_cache != prob.k_cache).any(axis=2)).tolist()}
+        assert changed == set(expect), (kv, sorted(changed))
+        for (page, slot), r in expect.items():
+            if kv == "e4m3":
+                codes, sc = orc.quantize_key(k_new[r])
+                assert np.array_equal(out.k_cache[page, slot], codes) and out.k_scale[page, slot] == sc
+            else:
+                assert np.array_equal(out.k_cache[page, slot], k_new[r])
+        if kv == "e4m3":
+            moved = {tuple(c) for c in np.argwhere(out.k_scale != prob.k_scale).tolist()}
+            assert moved <= set(expect), sorted(moved)
 
 
 ALL_PINS = [

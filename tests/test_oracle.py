@@ -50,6 +50,13 @@ MUTATIONS = [
     ("encode_bias", "(uint8_t)((e + 7) << 3)", "(uint8_t)((e + 8) << 3)"),
     ("encode_subnormal_step", "const double m = rint(ldexp(a, 9));", "const double m = rint(ldexp(a, 8));"),
     ("key_scale_unscaled", "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;", "const float sc = amax > 0.0f ? amax : 1.0f;"),
+    ("new_key_page_by_slot", "*page = page_table[(int64_t)row_req[r] * pt_stride + t / ORACLE_PAGE];",
+     "*page = page_table[(int64_t)row_req[r] * pt_stride + t % ORACLE_PAGE];"),
+    ("new_key_slot_by_page", "*slot = t % ORACLE_PAGE;", "*slot = t / ORACLE_PAGE;"),
+    ("new_key_at_bound", "const int64_t t = (int64_t)row_bound[r] - 1;", "const int64_t t = (int64_t)row_bound[r];"),
+    ("new_key_row_as_request", "page_table[(int64_t)row_req[r] * pt_stride + t / ORACLE_PAGE]",
+     "page_table[(int64_t)r * pt_stride + t / ORACLE_PAGE]"),
+    ("new_key_for_bound_zero", "    if (row_bound[r] == 0) return 0;\n", ""),
 ]
 
 
