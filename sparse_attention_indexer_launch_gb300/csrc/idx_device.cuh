@@ -198,6 +198,19 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---------------------------------------------------------------------------- registers
+// Per-warpgroup register budget (every warp of the warpgroup executes the same
+// call): release lowers this warpgroup's registers per thread to N, acquire
+// raises them to N, waiting until other warpgroups have released enough.
+template <int N>
+__device__ __forceinline__ void reg_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzled
 // canonical layout: rows of 128 bytes, groups of 8 rows 1024 bytes apart.
@@ -294,6 +307,26 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr)
       : "memory");
+}
+
+// 16 lanes x 256 bits (eight 32-bit columns), four repetitions along the columns.
+// Thread i of the warp receives, for repetition k (columns col + 8k .. col + 8k + 7):
+//   r[4k + 0], r[4k + 1]: lane (lane field + i / 4),     columns 8k + 2 (i % 4) + {0, 1};
+//   r[4k + 2], r[4k + 3]: lane (lane field + i / 4 + 8), the same columns.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

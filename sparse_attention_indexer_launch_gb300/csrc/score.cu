@@ -14,20 +14,21 @@
 // the launch's tiles; a tile is 128 consecutive key positions (two pages) of one
 // row group (up to 4 rows of one request).  For a tile the contraction is
 //     D[key][row*64 + head] = <k_key, q_row_head>      (M = 128, N = 64 * rows)
-// so a TMEM lane holds one key and each epilogue thread reduces its key's 64
-// head values of a row in registers.
+// so a TMEM lane holds one key; the 64 head values of a (key, row) are reduced by
+// four threads of one warp.
 //   warp 0      producer (with warp 18 for an E4M3 cache: even / odd tiles):
 //               page ids (32 per lane load, a block ahead), TMA of the
 //               key pages into an smem ring, the keys' scales into a second ring
 //               (two 256-byte bulk copies per tile), and the group's query operand
 //               (bulk copy) on group changes;
-//   warp 1      MMA issuer (one thread) and TMEM owner; two accumulators in TMEM,
-//               so the MMA of tile k+1 runs while tile k's epilogue reads;
-//   warps 2..17 epilogue, two groups of eight taking alternate tiles (group g
-//               reads accumulator g), four warps per TMEM lane quarter; each warp
-//               reduces two rows of its group's tiles for its quarter, so the
-//               per-tile costs (waits, scales, hand-back) are paid once per two
-//               rows and the groups work out of step with each other.
+//   warp 1      MMA issuer (lane 0) and TMEM owner; two accumulators in TMEM,
+//               so the MMA of tile k+1 runs while tile k's epilogue reads; with an
+//               E4M3 cache lane 0 of warp 19 issues the odd tiles' MMAs;
+//   warps 2..17 epilogue: every warp takes every tile, one row for its TMEM lane
+//               quarter (warp % 4), reading the row's 64 columns in the 16x256b
+//               shape so that each thread needs only 16 of the row's weights
+//               (held in registers), and hands the accumulator back right after
+//               its last TMEM read.
 // E4M3 cache: keys feed tcgen05.mma kind::f8f6f4 straight from the TMA ring; the
 // query is split exactly into two E4M3 terms (prep.cu), run as K = 2 x 128.
 // bf16 cache: keys and query are bf16, kind::f16, K = 128.
@@ -39,10 +40,16 @@ namespace {
 
 constexpr int kEpiWarps = 16;
 constexpr int kProducers = 2;                  // producer warps for an E4M3 cache
-constexpr int kProducer2Warp = 2 + kEpiWarps;  // the second one, after the epilogue warps
-constexpr int kThreads = 64 + kEpiWarps * 32 + 32;
+constexpr int kEpiWarp0 = 2;                            // warps 2 .. 17: the epilogue
+constexpr int kProducer2Warp = kEpiWarp0 + kEpiWarps;   // the second producer, after the epilogue warps
+constexpr int kMma2Warp = kProducer2Warp + 1;           // the second MMA issuer (odd tiles)
+constexpr int kThreads = (kMma2Warp + 1) * 32;
+template <int KV>
+constexpr int kIssuers = KV == IDX_KV_E4M3 ? 2 : 1;   // MMA-issuing threads
 constexpr int kBOperandBytes = 2 * kMaxGroupRows * kRowOperandBytes;  // two K blocks
-constexpr int kTmemCols = 512;                                        // two accumulators of 256
+constexpr int kSlots = 2;                    // accumulators in TMEM, used alternately
+constexpr int kSlotCols = 256;               // one tile: up to four rows x 64 heads
+constexpr int kTmemCols = kSlots * kSlotCols;
 constexpr int kScaleSlots = 8;
 constexpr int kHistWords = kHistBins / 2;   // two 16-bit counters per word
 constexpr int kFlushTiles = 256;            // 256 tiles x 128 keys < 65536: no counter overflows
@@ -59,8 +66,8 @@ struct Barriers {
   uint64_t empty[8];
   uint64_t sfull[kScaleSlots];
   uint64_t sempty[kScaleSlots];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[kSlots];
+  uint64_t tempty[kSlots];
   uint64_t bfull;
   uint64_t bfree;
   uint64_t drain;
@@ -76,8 +83,7 @@ struct Smem {
   static constexpr int kA = kB + kBOperandBytes;
   static constexpr int kHist = kA + Cfg<KV>::kStages * Cfg<KV>::kStageBytes;
   static constexpr int kScales = kHist + kMaxGroupRows * kHistWords * 4;
-  static constexpr int kW = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
-  static constexpr int kBars = kW + kEpiWarps * 2 * kHeads * 4;
+  static constexpr int kBars = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
   static constexpr int kBytes = kBars + static_cast<int>(sizeof(Barriers));
   static constexpr int kDynamic = kBytes + 1024;  // alignment slack
 };
@@ -117,41 +123,64 @@ __device__ __forceinline__ void set_abort(Barriers *bars, uint32_t *status) {
   *reinterpret_cast<volatile int *>(&bars->abort) = 1;
 }
 
-// sum_h w[h] * relu(v[h]) over 32 heads, with the weights already halved:
-// v + |v| = 2 relu(v) exactly, one FADD (the |v| is an operand modifier) on the
-// FMA pipe instead of a max on the ALU pipe, then packed FMAs into four
-// accumulators so that the FMAs of one row form four short chains.
-__device__ __forceinline__ void relu_dot32(const uint32_t (&v)[32], const float4 *w, float2 (&acc)[4]) {
+// One row's 16x256b.x4 fragment pair folded into the four keys' running sums.
+// Fragment va holds keys lane/4 (registers 4k, 4k+1) and lane/4 + 8 (4k+2,
+// 4k+3), vb the keys 16 lanes further on; repetition k holds heads
+// 8k + 2 (lane % 4) + {0, 1} of the half, whose halved weights are w[k].
+// v + |v| = 2 relu(v) exactly: one FADD on the FMA pipe (|v| is an operand
+// modifier), then a packed FMA per head pair.
+__device__ __forceinline__ void relu_frag(const uint32_t (&va)[16], const uint32_t (&vb)[16], const float2 *w,
+                                          float2 (&a)[4]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float4 wv = w[c];
-    float e[4];
+  for (int k = 0; k < 4; ++k) {
+    float e[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float d = __uint_as_float(v[4 * c + i]);
-      e[i] = d + fabsf(d);
+      const float x = __uint_as_float(va[4 * k + i]);
+      const float y = __uint_as_float(vb[4 * k + i]);
+      e[i] = x + fabsf(x);
+      e[4 + i] = y + fabsf(y);
     }
-    acc[(2 * c) & 3] = __ffma2_rn(make_float2(e[0], e[1]), make_float2(wv.x, wv.y), acc[(2 * c) & 3]);
-    acc[(2 * c + 1) & 3] = __ffma2_rn(make_float2(e[2], e[3]), make_float2(wv.z, wv.w), acc[(2 * c + 1) & 3]);
+    a[0] = __ffma2_rn(make_float2(e[0], e[1]), w[k], a[0]);
+    a[1] = __ffma2_rn(make_float2(e[2], e[3]), w[k], a[1]);
+    a[2] = __ffma2_rn(make_float2(e[4], e[5]), w[k], a[2]);
+    a[3] = __ffma2_rn(make_float2(e[6], e[7]), w[k], a[3]);
   }
 }
 
-// ReLU(s * d) = s * min(d, 0) for a negative scale s: the other branch
-// (d - |d| = 2 min(d, 0), again with the halved weights).
-__device__ __forceinline__ void relu_dot32_signed(const uint32_t (&v)[32], const float4 *w, bool neg,
-                                                  float2 (&acc)[4]) {
+// As relu_frag, with ReLU(s d) = s min(d, 0) for the keys whose scale s is
+// negative (neg bit m for key m): there the other branch, d - |d| = 2 min(d, 0).
+__device__ __forceinline__ void relu_frag_signed(const uint32_t (&va)[16], const uint32_t (&vb)[16],
+                                                 const float2 *w, uint32_t neg, float2 (&a)[4]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float4 wv = w[c];
-    float e[4];
+  for (int k = 0; k < 4; ++k) {
+    float e[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float d = __uint_as_float(v[4 * c + i]);
-      e[i] = neg ? d - fabsf(d) : d + fabsf(d);
+      const float x = __uint_as_float(va[4 * k + i]);
+      const float y = __uint_as_float(vb[4 * k + i]);
+      e[i] = ((neg >> (i >> 1)) & 1u) ? x - fabsf(x) : x + fabsf(x);
+      e[4 + i] = ((neg >> (2 + (i >> 1))) & 1u) ? y - fabsf(y) : y + fabsf(y);
     }
-    acc[0] = __ffma2_rn(make_float2(e[0], e[1]), make_float2(wv.x, wv.y), acc[0]);
-    acc[1] = __ffma2_rn(make_float2(e[2], e[3]), make_float2(wv.z, wv.w), acc[1]);
+    a[0] = __ffma2_rn(make_float2(e[0], e[1]), w[k], a[0]);
+    a[1] = __ffma2_rn(make_float2(e[2], e[3]), w[k], a[1]);
+    a[2] = __ffma2_rn(make_float2(e[4], e[5]), w[k], a[2]);
+    a[3] = __ffma2_rn(make_float2(e[6], e[7]), w[k], a[3]);
   }
+}
+
+// The four threads 4g .. 4g+3 of a warp hold partial sums of the same four keys
+// (s[m] for key m); afterwards thread i holds the whole sum of key i % 4.
+__device__ __forceinline__ float reduce_quad(const float (&s)[4], int lane) {
+  const bool hi2 = (lane & 2) != 0;
+  float k0 = hi2 ? s[2] : s[0];
+  float k1 = hi2 ? s[3] : s[1];
+  k0 += __shfl_xor_sync(0xffffffffu, hi2 ? s[0] : s[2], 2);
+  k1 += __shfl_xor_sync(0xffffffffu, hi2 ? s[1] : s[3], 2);
+  const bool hi1 = (lane & 1) != 0;
+  float k = hi1 ? k1 : k0;
+  k += __shfl_xor_sync(0xffffffffu, hi1 ? k0 : k1, 1);
+  return k;
 }
 
 template <int KV>
@@ -159,14 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
                                                              const ScoreArgs a) {
   using C = Cfg<KV>;
   using S = Smem<KV>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned by pointer arithmetic on the shared array itself, so that the
+  // compiler keeps every pointer below in the shared address space
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *sB0 = smem + S::kB;                          // K block 0 of the group's query operand
   uint8_t *sB1 = smem + S::kB + kBOperandBytes / 2;     // K block 1
   uint8_t *sA = smem + S::kA;                           // key ring
   uint32_t *shist = reinterpret_cast<uint32_t *>(smem + S::kHist);   // [row][2048] packed 16-bit counts
   float *sscale = reinterpret_cast<float *>(smem + S::kScales);     // [slot][128]
-  float *sw = reinterpret_cast<float *>(smem + S::kW);              // [epilogue warp][64]
   Barriers *bars = reinterpret_cast<Barriers *>(smem + S::kBars);
 
   const int warp = threadIdx.x >> 5;
@@ -181,17 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     for (int s = 0; s < kScaleSlots; ++s) {
       mbar_init(&bars->sfull[s], 1);           // the producer's arrival; the copies complete by bytes
-      mbar_init(&bars->sempty[s], kEpiWarps / 2);   // the eight warps of the tile's group
+      mbar_init(&bars->sempty[s], kEpiWarps);   // every epilogue warp passes every tile
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->tfull[s], 1);
-      mbar_init(&bars->tempty[s], kEpiWarps / 2);
+      mbar_init(&bars->tempty[s], kEpiWarps);   // every epilogue warp reads every tile
     }
     mbar_init(&bars->hdone[0], kEpiWarps);
     mbar_init(&bars->hflushed[0], kEpiWarps);
     mbar_init(&bars->bfull, 1);
-    mbar_init(&bars->bfree, 1);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->bfree, kIssuers<KV>);   // every MMA issuer is done with the group's query operand
+    mbar_init(&bars->drain, kIssuers<KV>);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -370,85 +400,113 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     if (pp == 0 && nb > 0 && !mbar_wait(&bars->bfull, (nb - 1) & 1, limit, &never) && lane == 0)
       flag_status(ws.status, kStatusTimeout);
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      GroupCursor cur;
-      cur.seek(ws.groups, num_groups, static_cast<int>(t0));
-      int cur_g = -1, nswitch = 0;
-      uint32_t idesc = 0;
+  } else if (warp == 1 || warp == kMma2Warp) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Tile k of the CTA's sequence accumulates into TMEM slot k % 2 (N = 64 x the
+    // group's rows); its MMA waits for the epilogue of tile k - 2.  With an E4M3
+    // cache two threads issue the MMAs, lane 0 of warp 1 for the even tiles (slot
+    // 0, even key stages) and lane 0 of warp kMma2Warp for the odd ones (slot 1,
+    // odd stages), so that one thread's per-tile waits and bookkeeping overlap the
+    // other's issue; each stage and slot barrier then has one waiter, which the
+    // parity waits need.  With a bf16 cache (three stages) warp 1 issues them all.
+    // Every issuer walks every group that has tiles in the CTA's range, waiting
+    // for its query operand and releasing it afterwards, whether or not it has
+    // tiles of its own there.
+    constexpr int nis = kIssuers<KV>;
+    if (lane == 0 && (warp == 1 || nis == 2)) {
+      const int par = warp == 1 ? 0 : 1;
       const uint32_t fmt = KV == IDX_KV_E4M3 ? 0u : 1u;
       const uint64_t bdesc0 = umma_desc_sw128(smem_u32(sB0)), bdesc1 = umma_desc_sw128(smem_u32(sB1));
-      // stage s of tile k and its phase, kept incrementally (no division per tile);
-      // stage s's A descriptor is stage 0's plus s stages of bytes / 16
+      // stage s of tile k and its phase, kept incrementally; stage s's A descriptor
+      // is stage 0's plus s stages of bytes / 16
       const uint64_t adesc0 = umma_desc_sw128(smem_u32(sA));
-      int s = 0;
+      const int T0 = static_cast<int>(t0), T1 = static_cast<int>(t1);
+      int s = par;
       uint32_t sphase = 0;
-      int k = 0;
-      for (int64_t t = t0; t < t1; ++t, ++k) {
-        cur.advance(static_cast<int>(t));
-        if (cur.g != cur_g) {
-          if (cur_g >= 0) umma_commit(&bars->bfree);
-          if (!mbar_wait(&bars->bfull, nswitch & 1, limit, abort)) {
-            set_abort(bars, ws.status);
-            break;
-          }
-          ++nswitch;
-          cur_g = cur.g;
-          idesc = umma_idesc(fmt, 64u * ws.groups[cur_g].nrows);
-        }
-        const int acc = k & 1;
-        if (!mbar_wait(&bars->full[s], sphase, limit, abort) ||
-            !mbar_wait(&bars->tempty[acc], ((k >> 1) & 1) ^ 1, limit, abort)) {
-          set_abort(bars, ws.status);
+      int t = T0 + par;       // next tile of this issuer
+      int nswitch = 0;
+      bool ok = true;
+      GroupCursor cur;
+      cur.seek(ws.groups, num_groups, T0);
+      for (int g = cur.g; ok && g < num_groups; ++g) {
+        const int gbeg = ws.groups[g].tile_begin;
+        if (gbeg >= T1) break;
+        const int gend = g + 1 < num_groups ? ws.groups[g + 1].tile_begin : total_tiles;
+        if (gend <= gbeg) continue;          // no tiles: its operand is never loaded
+        if (!mbar_wait(&bars->bfull, nswitch & 1, limit, abort)) {
+          ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t d = tmem_base + acc * 256;
-        // descriptors of the K steps: the base descriptor plus the step's byte offset / 16
-        // (the start-address field holds address / 16; no carry out of it in 256 KB)
-        const uint64_t adesc = adesc0 + static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+        ++nswitch;
+        const uint32_t idesc = umma_idesc(fmt, 64u * static_cast<uint32_t>(ws.groups[g].nrows));
+        const int tend = gend < T1 ? gend : T1;
+        for (; t < tend; t += nis) {
+          const int k = t - T0;
+          const uint32_t slot = static_cast<uint32_t>(k) % kSlots;
+          if (!mbar_wait(&bars->full[s], sphase, limit, abort) ||
+              !mbar_wait(&bars->tempty[slot], ((static_cast<uint32_t>(k) / kSlots) & 1u) ^ 1u, limit, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + slot * kSlotCols;
+          // descriptors of the K steps: the base descriptor plus the step's byte offset / 16
+          // (the start-address field holds address / 16; no carry out of it in 256 KB)
+          const uint64_t adesc = adesc0 + static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t koff = (kk & 3) * 32;
-          const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + (koff >> 4);
-          if (KV == IDX_KV_E4M3) {
-            umma_f8(d, adesc + (koff >> 4), bd, idesc, kk > 0);
-          } else {
-            umma_f16(d, adesc + (((kk < 4 ? 0u : static_cast<uint32_t>(kTileKeys) * 128u) + koff) >> 4), bd, idesc,
-                     kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (kk & 3) * 32;
+            const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + (koff >> 4);
+            if (KV == IDX_KV_E4M3) {
+              umma_f8(d, adesc + (koff >> 4), bd, idesc, kk > 0);
+            } else {
+              umma_f16(d, adesc + (((kk < 4 ? 0u : static_cast<uint32_t>(kTileKeys) * 128u) + koff) >> 4), bd,
+                       idesc, kk > 0);
+            }
+          }
+          umma_commit(&bars->empty[s]);
+          if (!(a.stall_first_handoff && t == T0)) umma_commit(&bars->tfull[slot]);
+          s += nis;
+          if (s >= C::kStages) {
+            s -= C::kStages;
+            sphase ^= 1u;
           }
         }
-        umma_commit(&bars->empty[s]);
-        if (!(a.stall_first_handoff && k == 0)) umma_commit(&bars->tfull[acc]);
-        if (++s == C::kStages) {
-          s = 0;
-          sphase ^= 1u;
-        }
+        if (ok) umma_commit(&bars->bfree);   // this thread's MMAs of the group read the operand
       }
+      if (!ok) set_abort(bars, ws.status);
       // All MMAs issued by this thread complete before TMEM is released.
       umma_commit(&bars->drain);
       int never = 0;
       if (!mbar_wait(&bars->drain, 0, limit, &never)) flag_status(ws.status, kStatusTimeout);
     }
-  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
     // ------------------------------------------------------------------ epilogue
-    // Two groups of eight warps take alternate tiles (group g reads accumulator g);
-    // within a group each warp reduces two rows of the tile for its TMEM lane quarter.
-    const int ew = warp - 2;
+    // Every epilogue warp takes every tile: the four warps of a TMEM lane quarter
+    // reduce one row each, so a warp reduces the same row of every tile of a
+    // group.  TMEM is read in the 16x256b shape: a thread sees four keys of its
+    // quarter and a quarter of the row's heads, so it keeps just those heads'
+    // weights in registers; the four threads that share keys add their partial
+    // sums by shuffles, after which thread `lane` holds key kl of the quarter.
+    // The tile's accumulator goes back to the MMA issuer right after the warp's
+    // last TMEM read.  Tile and key indices are 32-bit (a launch has fewer than
+    // 2^31 of either).
+    const int ew = warp - kEpiWarp0;
     const int quarter = warp & 3;            // TMEM lane quarter this warp may read
-    const int slot = ew >> 2;                // 0..3 among the quarter's four warps
-    const int tg = slot & 1;                 // tile parity this warp handles
-    const int r0 = (slot >> 1) * 2;          // first of this warp's two group rows
-    float *myw = sw + ew * 2 * kHeads;       // the two rows' weights
+    const int row = ew >> 2;                 // group row this warp reduces
+    const int kl = (lane >> 2) + 8 * (lane & 3);
+    const int qk = quarter * 32 + kl;        // this thread's key within a tile
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(row * 64);
+    uint32_t *hrow = shist + row * kHistWords;
+    const float *sc = sscale + qk;
+    const int T0 = static_cast<int>(t0), T1 = static_cast<int>(t1);
     GroupCursor cur;
-    cur.seek(ws.groups, num_groups, static_cast<int>(t0));
-    int cur_g = -1;
-    Group grp;
-    grp.nrows = 0;
-    grp.row0 = 0;
-    bool mine[2] = {false, false};
-    int32_t bnd[2] = {0, 0};
+    cur.seek(ws.groups, num_groups, T0);
+    Group grp{};
+    bool mine = false;
+    int bnd = 0, gbegin = 0, next_fp = 0;
+    float *srow = a.scores;
+    float2 w2[8];          // halved weights of heads 8k + 2 (lane % 4) + {0, 1}, k = 0..7
     int flushes = 0;
     bool ok = true;
 
@@ -474,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         for (int i = 0; i < 4; ++i) {
           if (__ballot_sync(0xffffffffu, wv[i] != 0u) == 0u) continue;   // uniform for the warp
           const int b = b0 + i * kEpiWarps;
-          const int row = b >> 6, d = b & 63;
-          const int64_t grow = grp.row0 + row;
+          const int hr = b >> 6, d = b & 63;
+          const int64_t grow = grp.row0 + hr;
           const uint32_t lo = wv[i] & 0xFFFFu, hi = wv[i] >> 16;
           if (wv[i]) {
-            shist[row * kHistWords + d * 32 + lane] = 0u;
+            shist[hr * kHistWords + d * 32 + lane] = 0u;
             if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
             if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
           }
@@ -495,108 +553,99 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       ++flushes;
       return r;
     };
-
-    // The two groups see different tiles, so the flush points (every group start
-    // and every kFlushTiles tiles within a group; 16-bit counters) are defined on
-    // the CTA's tile sequence and every warp takes each of them, in order.
+    // A new group: whether it has this warp's row, that row's bound, score row and
+    // weights.
     auto load_group = [&]() {
       grp = ws.groups[cur.g];
-      __syncwarp();
+      mine = row < grp.nrows;
+      const int r = grp.row0 + (mine ? row : 0);
+      bnd = mine ? ws.bound_eff[r] : 0;
+      gbegin = grp.tile_begin;
+      srow = a.scores + static_cast<int64_t>(r) * a.ld;
+      const float2 *wr = reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(r) * kHeads);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        mine[i] = r0 + i < grp.nrows;
-        bnd[i] = mine[i] ? ws.bound_eff[grp.row0 + r0 + i] : 0;
-        if (mine[i]) {
-          const float2 v =
-              reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(grp.row0 + r0 + i) * kHeads)[lane];
-          reinterpret_cast<float2 *>(myw + i * kHeads)[lane] = v;
-        }
-      }
-      __syncwarp();
+      for (int k = 0; k < 8; ++k) w2[k] = wr[4 * k + (lane & 3)];
     };
-    int64_t done = t0;   // flush points at or before this tile are taken
-    auto catch_up = [&](int64_t upto) -> bool {   // takes every flush point p in (done, upto]
-      for (;;) {
-        const int64_t periodic =
-            grp.tile_begin + ((done - grp.tile_begin) / kFlushTiles + 1) * static_cast<int64_t>(kFlushTiles);
-        const int64_t p = periodic < cur.next_begin ? periodic : static_cast<int64_t>(cur.next_begin);
-        if (p > upto) break;
-        if (!flush()) return false;
-        if (p == cur.next_begin) {
-          cur.advance(static_cast<int>(p));
-          load_group();
-        }
-        done = p;
-      }
-      if (upto > done) done = upto;
-      return true;
+    // The histogram flush points: every group start and every kFlushTiles tiles
+    // within a group (16-bit counters), on the CTA's tile sequence; every warp
+    // takes each of them, in order, before the tile that starts there.
+    auto set_next_fp = [&](int t) {
+      const int periodic = gbegin + ((t - gbegin) / kFlushTiles + 1) * kFlushTiles;
+      next_fp = periodic < cur.next_begin ? periodic : cur.next_begin;
     };
     load_group();
-    cur_g = cur.g;
+    set_next_fp(T0);
 
-    for (int64_t t = t0 + tg; t < t1; t += 2) {
-      const int k = static_cast<int>(t - t0);
-      if (!catch_up(t)) {
-        ok = false;
-        break;
+    for (int t = T0; t < T1; ++t) {
+      if (t == next_fp) {
+        if (!flush()) {
+          ok = false;
+          break;
+        }
+        if (t == cur.next_begin) {
+          cur.advance(t);
+          load_group();
+        }
+        set_next_fp(t);
       }
-      const int j = static_cast<int>(t) - grp.tile_begin;
-      const int64_t pos = static_cast<int64_t>(j) * kTileKeys + quarter * 32 + lane;
-      const int acc = tg;
-      const int ss = k % kScaleSlots;
+      const int k = t - T0;
       float scale = 1.0f;
       if (KV == IDX_KV_E4M3) {
+        const int ss = k & (kScaleSlots - 1);
         if (!mbar_wait(&bars->sfull[ss], (k / kScaleSlots) & 1, limit, abort)) {
           set_abort(bars, ws.status);
           ok = false;
           break;
         }
-        scale = sscale[ss * kTileKeys + quarter * 32 + lane];
+        scale = sc[ss * kTileKeys];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->sempty[ss]);
       }
-      if (!mbar_wait(&bars->tfull[acc], (k >> 1) & 1, limit, abort)) {
+      const int slot = k & (kSlots - 1);
+      if (!mbar_wait(&bars->tfull[slot], (k / kSlots) & 1, limit, abort)) {
         set_abort(bars, ws.status);
         ok = false;
         break;
       }
       tc_fence_after();
-      float score[2] = {0.f, 0.f};
-      const bool valid = pos < grp.L;
-      const bool neg = valid && scale < 0.0f;
-      const bool any_neg = __any_sync(0xffffffffu, neg);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (!mine[i]) continue;            // uniform for the warp
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256 + (r0 + i) * 64;
-        const float4 *w4 = reinterpret_cast<const float4 *>(myw + i * kHeads);
-        float2 accs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld32(taddr + half * 32, v);
-          tmem_wait_ld();
-          reg_fence(v);
-          if (!any_neg) relu_dot32(v, w4 + half * 8, accs);
-          else relu_dot32_signed(v, w4 + half * 8, neg, accs);
-        }
-        score[i] = (((accs[0].x + accs[0].y) + (accs[1].x + accs[1].y)) + ((accs[2].x + accs[2].y) + (accs[3].x + accs[3].y))) * scale;
+      if (!mine) {   // the group has no row for this warp: hand the accumulator back at once
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+        continue;
       }
-      // Accumulator read: hand it back to the MMA issuer.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      const int pos = (t - gbegin) * kTileKeys + qk;
+      const bool keep = pos < bnd;   // below the row's bound (so also below the group's L)
+      // bit (4g + m) set: key m of threads 4g .. 4g+3 (quarter lane g + 8m) has a negative scale
+      const uint32_t negmask = __ballot_sync(0xffffffffu, keep && scale < 0.0f);
+      const uint32_t taddr = tq + static_cast<uint32_t>(slot * kSlotCols);
+      float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (!mine[i]) continue;
-        const bool keep = valid && pos < bnd[i];
-        if (keep) a.scores[static_cast<int64_t>(grp.row0 + r0 + i) * a.ld + pos] = score[i];
-        const uint32_t bin = radix_key(score[i]) >> (32 - kHistBits);
-        uint32_t *h = shist + (r0 + i) * kHistWords;
-        if (keep) atomicAdd(&h[bin >> 1], 1u << ((bin & 1) * 16));   // shared-memory atomics resolve collisions
+      for (int half = 0; half < 2; ++half) {
+        uint32_t va[16], vb[16];
+        tmem_ld16x256_x4(taddr + half * 32, va);
+        tmem_ld16x256_x4(taddr + (16u << 16) + half * 32, vb);
+        tmem_wait_ld();
+        reg_fence16(va);
+        reg_fence16(vb);
+        if (half == 1) {   // every read of this warp is done: hand the accumulator back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+        }
+        if (negmask == 0u) relu_frag(va, vb, &w2[4 * half], sums);
+        else relu_frag_signed(va, vb, &w2[4 * half], (negmask >> (lane & ~3)) & 15u, sums);
+      }
+      const float part[4] = {sums[0].x + sums[0].y, sums[1].x + sums[1].y, sums[2].x + sums[2].y,
+                             sums[3].x + sums[3].y};
+      const float score = reduce_quad(part, lane) * scale;
+      if (keep) {
+        srow[pos] = score;
+        const uint32_t bin = radix_key(score) >> (32 - kHistBits);
+        atomicAdd(&hrow[bin >> 1], 1u << ((bin & 1) * 16));   // shared-memory atomics resolve collisions
       }
     }
-    if (ok && catch_up(t1 - 1)) flush();
+    if (ok) flush();
   }
 
   // Every role is done (or gave up); release TMEM.
