@@ -173,6 +173,29 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
       : "memory");
 }
 
+// Bulk reduction shared -> global: dst[i] += src[i] for `bytes` / 4 u32 words,
+// element by element atomically, by the TMA engine (16-byte aligned addresses,
+// size a multiple of 16).  One bulk group per call; the generic-proxy writes of
+// src must be made visible to the async proxy first (fence_proxy_async_shared).
+__device__ __forceinline__ void bulk_reduce_add_u32(uint32_t *gdst, const uint32_t *ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Programmatic dependent launch: wait until the grid this launch depends on has
 // completed and its memory is visible (a no-op when launched without the attribute).
 __device__ __forceinline__ void grid_dependency_wait() {

@@ -53,6 +53,7 @@ constexpr int kTmemCols = kSlots * kSlotCols;
 constexpr int kScaleSlots = 8;
 constexpr int kHistWords = kHistBins / 2;   // two 16-bit counters per word
 constexpr int kFlushTiles = 256;            // 256 tiles x 128 keys < 65536: no counter overflows
+constexpr int kStageBlocks = 4;             // histogram blocks each epilogue warp has in flight to global
 
 template <int KV>
 struct Cfg {
@@ -83,7 +84,8 @@ struct Smem {
   static constexpr int kA = kB + kBOperandBytes;
   static constexpr int kHist = kA + Cfg<KV>::kStages * Cfg<KV>::kStageBytes;
   static constexpr int kScales = kHist + kMaxGroupRows * kHistWords * 4;
-  static constexpr int kBars = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
+  static constexpr int kFlushStage = kScales + (KV == IDX_KV_E4M3 ? kScaleSlots * kTileKeys * 4 : 0);
+  static constexpr int kBars = kFlushStage + kEpiWarps * kStageBlocks * 64 * 4;
   static constexpr int kBytes = kBars + static_cast<int>(sizeof(Barriers));
   static constexpr int kDynamic = kBytes + 1024;  // alignment slack
 };
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   uint8_t *sA = smem + S::kA;                           // key ring
   uint32_t *shist = reinterpret_cast<uint32_t *>(smem + S::kHist);   // [row][2048] packed 16-bit counts
   float *sscale = reinterpret_cast<float *>(smem + S::kScales);     // [slot][128]
+  uint32_t *sflush = reinterpret_cast<uint32_t *>(smem + S::kFlushStage);   // [epilogue warp][4][64]
   Barriers *bars = reinterpret_cast<Barriers *>(smem + S::kBars);
 
   const int warp = threadIdx.x >> 5;
@@ -515,12 +518,17 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // sixteen warps meet before and after.  The group's nrows x 64 (row, first digit)
     // blocks of 64 bins are dealt round-robin to the warps, four at a time: the four
     // shared-memory reads go out together, and a block with no count (most of them:
-    // a CTA's scores fill a few hundred of a row's 4096 bins) costs one vote.
+    // a CTA's scores fill a few hundred of a row's 4096 bins) costs one vote.  A
+    // block with counts is unpacked into one of the warp's staging slots and added
+    // to the row's 12-bit histogram by one bulk reduction (the TMA engine performs
+    // the 64 additions); its sum goes to the first digit by one atomic.
+    uint32_t *stage = sflush + ew * (kStageBlocks * 64);
     auto flush = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->hdone[0]);
       if (!mbar_wait(&bars->hdone[0], flushes & 1, limit, abort)) return false;
       const int nblk = grp.nrows * 64;
+      int staged = 0;
       for (int b0 = ew; b0 < nblk; b0 += 4 * kEpiWarps) {
         uint32_t wv[4];
 #pragma unroll
@@ -535,18 +543,25 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           const int hr = b >> 6, d = b & 63;
           const int64_t grow = grp.row0 + hr;
           const uint32_t lo = wv[i] & 0xFFFFu, hi = wv[i] >> 16;
-          if (wv[i]) {
-            shist[hr * kHistWords + d * 32 + lane] = 0u;
-            if (lo) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane], lo);
-            if (hi) atomicAdd(&ws.hist12[grow * kHistBins + d * 64 + 2 * lane + 1], hi);
+          if (staged >= kStageBlocks) {   // the slot's previous block must have been read
+            if (lane == 0) bulk_wait_read<kStageBlocks - 1>();
+            __syncwarp();
           }
+          uint32_t *slot = stage + (staged % kStageBlocks) * 64;
+          reinterpret_cast<uint2 *>(slot)[lane] = make_uint2(lo, hi);
+          shist[hr * kHistWords + d * 32 + lane] = 0u;
           const uint32_t dsum = __reduce_add_sync(0xffffffffu, lo + hi);
+          fence_proxy_async_shared();
+          __syncwarp();
           if (lane == 0) {
+            bulk_reduce_add_u32(&ws.hist12[grow * kHistBins + d * 64], slot, 256u);
             atomicAdd(&ws.hist64[grow * 64 + d], dsum);
             if (a.hist != nullptr) atomicAdd(&a.hist[grow * 64 + d], dsum);
           }
+          ++staged;
         }
       }
+      if (lane == 0 && staged > 0) bulk_wait_all();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->hflushed[0]);
       const bool r = mbar_wait(&bars->hflushed[0], flushes & 1, limit, abort);
