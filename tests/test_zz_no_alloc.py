@@ -1,6 +1,7 @@
 """idx_topk_noalloc (top-K on the library's own scratch, no caller workspace)
-against idx_topk on the same scores: two different calls in a row, each equal to
-idx_topk's result, and the row limit refused before anything is launched.
+against idx_topk and the oracle's selection on the same scores: two different
+calls in a row, each equal to both, and the row limit refused before anything is
+launched.
 
 Collected last on purpose, so that it also runs after every other GPU test of
 the session has used the device."""
@@ -48,15 +49,17 @@ def _pair(lib, s, bounds, K):
     return ref.cpu().numpy(), got.cpu().numpy()
 
 
-def test_noalloc_matches_idx_topk_on_two_calls_in_a_row(lib):
+def test_noalloc_matches_idx_topk_on_two_calls_in_a_row(lib, orc):
     # first call: 8 rows (the limit), K = 2048
     s1, b1 = _scores(101, MAX_ROWS, 40000)
     ref1, got1 = _pair(lib, s1, b1, 2048)
     assert np.array_equal(got1, ref1)
+    assert np.array_equal(got1, orc.topk(s1, b1, 2048))
     # second call right after, other shapes and scores: nothing may leak from the first
     s2, b2 = _scores(202, 6, 9000)
     ref2, got2 = _pair(lib, s2, b2, 100)
     assert np.array_equal(got2, ref2)
+    assert np.array_equal(got2, orc.topk(s2, b2, 100))
     assert (got2[4] == -1).all()                       # the empty row is all padding
 
 
