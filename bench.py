@@ -348,6 +348,48 @@ def run_patch(args):
     return 0
 
 
+def time_config(lib, prob, steps, warmup, flush, stream):
+    """One workload timed as the main line is: L2 flushed before every step, CUDA
+    events around the launch on its stream, every other step also timing the
+    scoring kernel.  Returns (launch ms, scoring-kernel ms)."""
+    import torch
+    dp = lib.DeviceProblem(prob)
+    out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
+    for _ in range(warmup):
+        flush.zero_()
+        dp.launch(out)
+    torch.cuda.synchronize()
+    st = dp.status()
+    if st != lib.IDX_OK:
+        raise SystemExit(f"device status ({prob.name}): {lib.status_string(st)}")
+    pairs = []
+    for i in range(steps):
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        sev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in (*ev, *sev):
+            e.record(stream)
+        flush.zero_()
+        if i % 2 == 1:
+            lib.profile_next_score(sev[0], sev[1])
+        ev[0].record(stream)
+        dp.launch(out)
+        ev[1].record(stream)
+        pairs.append((i, ev, sev))
+    torch.cuda.synchronize()
+    launch = [ev[0].elapsed_time(ev[1]) for i, ev, _ in pairs if i % 2 == 0]
+    score = [sev[0].elapsed_time(sev[1]) for i, _, sev in pairs if i % 2 == 1]
+    return statistics.mean(launch), statistics.mean(score)
+
+
+def roofline_terms(prob, hbm_gbs, bf16_tf):
+    """(launch roofline s, bound, FP8 TF/s) of a workload: max(key bytes / HBM,
+    MMA flops / FP8 peak), FP8 taken as twice the measured bf16 rate."""
+    fp8_tf = 2.0 * bf16_tf
+    t_hbm = prob.key_bytes / (hbm_gbs * 1e9)
+    t_fp8 = prob.mma_flops / (fp8_tf * 1e12)
+    return max(t_hbm, t_fp8), ("hbm" if t_hbm >= t_fp8 else "tensor"), fp8_tf
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -357,6 +399,9 @@ def main():
     ap.add_argument("--config", default="3", help="workload: 0..4, 3a or 3b (default 3)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--extra-configs", default="3a",
+                    help="comma-separated workloads also timed (same protocol) and reported under "
+                         "extra_configs; 'none' for none")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds for the whole --impl reference run")
     ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch"],
@@ -488,17 +533,32 @@ def main():
         ms, score_mean_ms, e2e_ms = max_over_ranks([ms, score_mean_ms, e2e_ms or 0.0], "cuda")
         e2e_ms = e2e_ms or None
 
+    # the other workloads of the metric's target (same protocol, after the main
+    # timed region; rank 0 reports them)
+    hbm_gbs, bf16_tf, peak_src = measured_peaks()
+    extra = []
+    for name in [c.strip() for c in args.extra_configs.split(",") if c.strip() and c.strip() != "none"]:
+        ecfg = name if name in ("3a", "3b") else int(name)
+        if ecfg == cfg:
+            continue
+        eprob = rank_problem(ecfg, rank)
+        e_ms, e_score_ms = time_config(lib, eprob, max(2, min(args.steps, 400)), args.warmup, flush, stream)
+        e_roof, e_bound, _ = roofline_terms(eprob, hbm_gbs, bf16_tf)
+        extra.append({"workload": workloads.CONFIG_NAMES[ecfg], "us_per_launch": e_ms * 1e3,
+                      "value": eprob.key_rows / (e_ms * 1e-3), "unit": "key·rows/s",
+                      "kernel_us": e_score_ms * 1e3, "launch_roofline_us": e_roof * 1e6, "bound": e_bound,
+                      "launch_frac_of_roofline": e_roof / (e_ms * 1e-3),
+                      "kernel_frac_hbm": eprob.key_bytes / (e_score_ms * 1e-3) / 1e9 / hbm_gbs,
+                      "tensor_frac_bf16_precision_matched":
+                          eprob.mma_flops / (e_score_ms * 1e-3) / 1e12 / bf16_tf})
+        del eprob
+
     key_rows_total = total_key_rows(prob.key_rows, world)
     value = key_rows_total / (ms * 1e-3)
-    hbm_gbs, bf16_tf, peak_src = measured_peaks()
-    fp8_tf = 2.0 * bf16_tf     # FP8 dense = 2 x bf16 dense (nominal ratio)
     key_bytes = prob.key_bytes
     flops = prob.mma_flops
     # The metric's roofline: max(key bytes / HBM, FP8 flops / FP8 peak).
-    t_hbm = key_bytes / (hbm_gbs * 1e9)
-    t_fp8 = flops / (fp8_tf * 1e12)
-    t_roof = max(t_hbm, t_fp8)
-    bound = "hbm" if t_hbm >= t_fp8 else "tensor"
+    t_roof, bound, fp8_tf = roofline_terms(prob, hbm_gbs, bf16_tf)
     score_s = score_mean_ms * 1e-3
     if bound == "hbm":
         achieved, peak, unit = key_bytes / score_s / 1e9, hbm_gbs, "GB/s"
@@ -533,6 +593,8 @@ def main():
                        "l2": "flushed before every step (256 MB write)"},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": traffic,
+                         "frac_scope": "the scoring kernel alone (the dominant kernel); "
+                                       "launch_frac_of_roofline is the whole launch",
                          "kernel": "score_kernel (scan + contraction + head reduction + histogram)",
                          "kernel_us": score_mean_ms * 1e3,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json; FP8 = 2 x bf16)",
@@ -546,6 +608,8 @@ def main():
             "gpu_launches": KERNELS_PER_LAUNCH * args.steps,
             "wall_s_timed_region": t_wall,
         }
+        if extra:
+            line["extra_configs"] = extra
         if e2e_ms is not None:
             line["e2e"] = {"value": key_rows_total / (e2e_ms * 1e-3), "unit": "key·rows/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}

@@ -217,7 +217,10 @@ idx_status idx_top1(const float *logits, int64_t ld, int32_t R, int64_t V, int32
  *   Setup: the first call on a device looks up the scratch's device address
  *   (cudaGetSymbolAddress) and keeps it for later calls; make that first call on
  *   each device before any stream capture begins.  A failed lookup returns
- *   IDX_ECUDA.
+ *   IDX_ECUDA.  The kept address belongs to the device's context as it was at
+ *   that first call: after a cudaDeviceReset (or anything else that destroys and
+ *   recreates the device's primary context) the process must be restarted before
+ *   this call is used on that device again.
  *   Nothing in the scratch has to start at zero: every call clears the selection
  *   state it uses before its kernels read it.
  *   The scratch is one per device and process: two calls whose work can overlap

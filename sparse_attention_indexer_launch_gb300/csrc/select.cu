@@ -269,7 +269,12 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   if (a.bulk_rows) {
     if (!mbar_wait(&bar, 0, a.wait_limit_ns, &abort_flag)) {
       flag_status(ws.status, kStatusTimeout);
-      return;   // the copy's completion is not awaited further: the status reports the launch failed
+      // The status reports the launch failed.  Before the CTA's shared memory is
+      // released, wait once more (again with a limit) for the copy still in
+      // flight to land.
+      int never = 0;
+      mbar_wait(&bar, 0, a.wait_limit_ns, &never);
+      return;
     }
   } else {
     __syncthreads();

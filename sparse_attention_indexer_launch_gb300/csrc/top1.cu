@@ -1,14 +1,17 @@
 // Top-1 of each row of logits in one launch.
 //
-// sglang PR 48224 page, later commit on the same page ("draft_topk1_postprocess
-// reduced each row in a split pass and a finalize launch"): every split of a row
-// folds its (value, lowest index) into one 64-bit key per row with an atomic
-// maximum, and the split that arrives last writes the row's results and resets
-// the row's state, so one launch does both.  Ties go to the lowest index and a
-// NaN reads as -1e30.
+// The sglang PR 48224 page, later commit on the draft top-1 postprocess: the
+// page's version made two launches per step (a pass over splits of each row,
+// then a finalizing one).  Here a single launch covers both.  Each CTA takes a
+// split of a row, finds its best (value, position) pair, and merges it into the
+// row's running best with one 64-bit atomicMax.  An arrival counter per row
+// tells the CTA that merges last; that CTA writes the row's outputs and zeroes
+// the row's state for the next call.  Equal values resolve to the smaller
+// position, and a NaN logit counts as -1e30, as on the page.
 //
-// The key is (radix_key(value) << 32) | ~index: a larger value wins, and among
-// equal values (-0.0 and +0.0 are equal) the lower index has the larger ~index.
+// The packed key is (radix_key(value) << 32) | ~position: the order-preserving
+// radix key makes a larger value win, and for equal values (with -0.0 equal to
+// +0.0) the complemented position is larger for the smaller position.
 #include "idx_device.cuh"
 #include "launch.h"
 
