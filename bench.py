@@ -390,6 +390,58 @@ def roofline_terms(prob, hbm_gbs, bf16_tf):
     return max(t_hbm, t_fp8), ("hbm" if t_hbm >= t_fp8 else "tensor"), fp8_tf
 
 
+def run_merge(args):
+    """--op merge: idx_merge_topk of S ranked parts of R rows x K (the key-sharded
+    indexer's owner merge), S = 2, 4, 8; CUDA events around each call, L2 flushed
+    before each.  The parts are every row's top-K of S disjoint ranges of 524,288
+    normal scores, ranked by the oracle."""
+    import numpy as np
+    import torch
+    import oracle
+    import sparse_attention_indexer_launch_gb300 as lib
+    orc = oracle.default()
+    R, K, L = 8, 2048, 524288
+    rng = np.random.default_rng(13)
+    scores = rng.standard_normal((R, L)).astype(np.float32)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = {}
+    for S in (2, 4, 8):
+        cuts = [L * i // S for i in range(S + 1)]
+        pi = np.full((S, R, K), -1, np.int32)
+        ps = np.full((S, R, K), -np.inf, np.float32)
+        for i in range(S):
+            sub = np.ascontiguousarray(scores[:, cuts[i]:cuts[i + 1]])
+            idx = orc.topk(sub, np.full(R, cuts[i + 1] - cuts[i], np.int32), K)
+            pi[i] = idx
+            ps[i] = np.take_along_axis(sub, np.maximum(idx, 0), axis=1)
+        dpi, dps = torch.from_numpy(pi).cuda(), torch.from_numpy(ps).cuda()
+        out = torch.empty((R, K), dtype=torch.int32, device="cuda")
+        for _ in range(args.warmup):
+            lib.idx_merge_topk(dpi, dps, cuts[:-1], K, out)
+        torch.cuda.synchronize()
+        want = orc.topk(scores, np.full(R, L, np.int32), K)
+        if not np.array_equal(out.cpu().numpy(), want):
+            raise SystemExit(f"idx_merge_topk of {S} parts differs from the unsharded selection")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            lib.idx_merge_topk(dpi, dps, cuts[:-1], K, out)
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        t0 = time.perf_counter()
+        orc.merge_topk(pi, ps, np.array(cuts[:-1], np.int32), K)
+        res[S] = {"us": us, "oracle_us": (time.perf_counter() - t0) * 1e6, "bytes_in": pi.nbytes + ps.nbytes}
+    print(json.dumps({"metric": "µs per owner merge of S ranked parts (8 rows x top-2048)", "op": "merge",
+                      "value": res[2]["us"], "unit": "µs", "higher_is_better": False, "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "parts": res,
+                      "config": {"workload": "8 rows x 524,288 N(0,1) scores split into S ranges",
+                                 "l2": "flushed before every call (256 MB write)"}}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,9 +456,9 @@ def main():
                          "extra_configs; 'none' for none")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds for the whole --impl reference run")
-    ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch"],
+    ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch", "merge"],
                     help="indexer: the fused indexer launch (the benchmark); top1: the one-launch top-1; "
-                         "patch: the new-key patch")
+                         "patch: the new-key patch; merge: the key-sharded owner merge")
     ap.add_argument("--top1-rows", type=int, default=8)
     ap.add_argument("--top1-vocab", type=int, default=151552)
     args = ap.parse_args()
@@ -419,6 +471,8 @@ def main():
         return run_top1(args)
     if args.op == "patch":
         return run_patch(args)
+    if args.op == "merge":
+        return run_merge(args)
 
     import numpy as np
     import torch

@@ -126,6 +126,38 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
 idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws,
                       size_t ws_bytes, void *stream);
 
+/* idx_launch that also returns the selected keys' scores (the first half of a
+ * key-sharded indexer: each shard ranks the keys it holds; see idx_merge_topk).
+ *   out_score  device fp32 [R][K]: out_score[r][j] is the score of position
+ *              out_idx[r][j] (-0.0 comes back as +0.0); -inf where out_idx is -1.
+ * Other arguments and errors as for idx_launch; a NULL out_score is IDX_EINVAL. */
+idx_status idx_launch_scored(const idx_problem *problem, int32_t K, int32_t *out_idx, float *out_score,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/* Exact top-K of the union of S ranked parts: the merge of a key-sharded indexer.
+ * The "Release Test Suite - GLM-5.2-EXL3" page (section Config change) runs decode
+ * context parallelism with a top-k owner merge: every GPU ranks the keys of its
+ * shard of the cache and one owner merges the lists.  The union of the shards'
+ * top-K lists holds the global top-K, so the merge reproduces the unsharded
+ * selection exactly.
+ *   part_idx     device int32 [S][R][Kin]: part s's positions in its own numbering,
+ *                ordered by score descending then position ascending, -1 padded
+ *                (as idx_launch_scored writes them).
+ *   part_score   device fp32 [S][R][Kin]: their scores (no NaN).
+ *   part_offset  HOST int32 [S], >= 0: added to part s's positions; the parts must
+ *                cover disjoint position ranges (a position of the request is in
+ *                exactly one part).
+ *   S            1 .. IDX_MERGE_MAX_PARTS; Kin, K in 1 .. IDX_MAX_K.
+ *   out_idx      device int32 [R][K]: the merged positions, same order, -1 padded.
+ *   out_score    device fp32 [R][K] or NULL: their scores, -inf where out_idx is -1.
+ * Returns IDX_EINVAL for a bad argument and IDX_EUNSUPPORTED for S or R above the
+ * limits; launches nothing then.
+ * Asynchronous on `stream`; allocates nothing. */
+#define IDX_MERGE_MAX_PARTS 8
+idx_status idx_merge_topk(const int32_t *part_idx, const float *part_score, const int32_t *part_offset,
+                          int32_t S, int32_t R, int32_t Kin, int32_t K, int32_t *out_idx, float *out_score,
+                          void *stream);
+
 /* Bytes of device arena idx_launch_host needs: the inputs' device copies, the
  * output and the workspace. */
 size_t idx_host_arena_size(const idx_problem *host_problem, int32_t K);

@@ -75,6 +75,8 @@ def _bind(path: str):
     lib.oracle_quantize_key.restype = None
     lib.oracle_patch_new_keys.argtypes = [p, p, p, i32, p, i64, i32, p, p, i32, i64]
     lib.oracle_patch_new_keys.restype = i32
+    lib.oracle_merge_topk.argtypes = [p, p, p, i32, i32, i32, i32, p]
+    lib.oracle_merge_topk.restype = i32
     lib.oracle_top1.argtypes = [p, i64, i32, i64, p, p]
     lib.oracle_top1.restype = None
     lib.oracle_num_threads.argtypes = []
@@ -162,6 +164,19 @@ class Oracle:
         rc = self.lib.oracle_topk(_ptr(s), s.shape[1], _ptr(rb), R, K, _ptr(out))
         if rc != 0:
             raise ValueError("oracle_topk: NaN score within a bound")
+        return out
+
+    def merge_topk(self, part_idx, part_score, offsets, K: int) -> np.ndarray:
+        """Exact top-K [R][K] of the union of S parts ([S][R][Kin] positions, -1 for
+        none, and scores), part s's positions shifted by offsets[s]."""
+        pi = _c(part_idx, np.int32)
+        ps = _c(part_score, np.float32)
+        off = _c(offsets, np.int32)
+        S, R, Kin = pi.shape
+        out = np.empty((R, K), dtype=np.int32)
+        rc = self.lib.oracle_merge_topk(_ptr(pi), _ptr(ps), _ptr(off), S, R, Kin, K, _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_merge_topk: NaN score")
         return out
 
     def radix_key(self, x) -> np.ndarray:

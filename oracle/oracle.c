@@ -341,6 +341,39 @@ int oracle_topk(const float *scores, int64_t ld, const int32_t *row_bound, int R
  * value.  Non-negative values get the sign bit set; negative values are bitwise
  * inverted.  -0.0 is first read as +0.0.  The page's first radix digit is this
  * key's top 6 bits, radix_key >> 26 (section Modifications, commit 4). */
+/* Merge of a key-sharded selection, by definition: the exact top-K of the union
+ * of S parts.  The "Release Test Suite - GLM-5.2-EXL3" page (section Config
+ * change) merges each GPU's indexer top-k at an owner under decode context
+ * parallelism.  Part s holds, for each row, up to Kin (score, position) pairs with
+ * positions in its own numbering (-1 marks an empty entry); global position =
+ * position + offset[s].  Every pair of every part is put in one list, ordered as
+ * oracle_topk orders (score descending by value, then position ascending), and
+ * the first K global positions are kept, -1 padded.
+ *   part_idx / part_score [S][R][Kin]; offset [S]; out_idx [R][K].
+ * Returns 0, or -1 if a listed score is NaN. */
+int oracle_merge_topk(const int32_t *part_idx, const float *part_score, const int32_t *offset, int S, int R,
+                      int Kin, int K, int32_t *out_idx) {
+    int bad = 0;
+    for (int r = 0; r < R; ++r) {
+        scored_key *v = (scored_key *)malloc(sizeof(scored_key) * (size_t)S * (size_t)Kin + 1);
+        int64_t n = 0;
+        for (int s = 0; s < S; ++s) {
+            for (int j = 0; j < Kin; ++j) {
+                const int64_t at = ((int64_t)s * R + r) * Kin + j;
+                if (part_idx[at] < 0) continue;
+                v[n].score = part_score[at];
+                v[n].pos = part_idx[at] + offset[s];
+                if (isnan(v[n].score)) bad = 1;
+                ++n;
+            }
+        }
+        qsort(v, (size_t)n, sizeof(scored_key), by_score_then_pos);
+        for (int j = 0; j < K; ++j) out_idx[(int64_t)r * K + j] = j < n ? v[j].pos : -1;
+        free(v);
+    }
+    return bad ? -1 : 0;
+}
+
 uint32_t oracle_radix_key(float x) {
     uint32_t u;
     if (x == 0.0f) x = 0.0f;

@@ -8,6 +8,8 @@ not been built, importing this package raises; there is no other code path.
     idx_topk    exact top-K positions of given scores
     idx_launch  both, fused on one stream
     idx_launch_host  idx_launch on host inputs, copies included
+    idx_launch_scored, idx_merge_topk  the key-sharded indexer (shard.py splits
+                     a problem and exchanges the shards' lists)
 """
 from __future__ import annotations
 
@@ -25,7 +27,7 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
            "idx_debug_set", "idx_profile_events", "idx_top1_state_size", "idx_top1", "idx_topk_noalloc",
-           "idx_patch_new_keys"]
+           "idx_patch_new_keys", "idx_launch_scored", "idx_merge_topk"]
 
 
 class IdxError(RuntimeError):
@@ -82,6 +84,10 @@ def _load():
     lib.idx_top1.restype = ctypes.c_int
     lib.idx_topk_noalloc.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp]
     lib.idx_topk_noalloc.restype = ctypes.c_int
+    lib.idx_launch_scored.argtypes = [P, i32, vp, vp, vp, sz, vp]
+    lib.idx_launch_scored.restype = ctypes.c_int
+    lib.idx_merge_topk.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), i32, i32, i32, i32, vp, vp, vp]
+    lib.idx_merge_topk.restype = ctypes.c_int
     return lib
 
 
@@ -172,6 +178,20 @@ def idx_launch(problem: Problem, K: int, out_idx, ws, stream=None):
                           ws.numel() * ws.element_size(), _stream(stream)), "idx_launch")
 
 
+def idx_launch_scored(problem: Problem, K: int, out_idx, out_score, ws, stream=None):
+    _check(lib.idx_launch_scored(ctypes.byref(problem), int(K), _ptr(out_idx), _ptr(out_score), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "idx_launch_scored")
+
+
+def idx_merge_topk(part_idx, part_score, offsets, K: int, out_idx, out_score=None, stream=None):
+    """part_idx / part_score: [S][R][Kin] device tensors (int32 / fp32); offsets: S
+    host integers; out_idx [R][K] (and out_score [R][K]) device tensors."""
+    S, R, Kin = (int(x) for x in part_idx.shape)
+    off = (ctypes.c_int32 * S)(*[int(o) for o in offsets])
+    _check(lib.idx_merge_topk(_ptr(part_idx), _ptr(part_score), off, S, R, Kin, int(K), _ptr(out_idx),
+                              _ptr(out_score), _stream(stream)), "idx_merge_topk")
+
+
 def idx_launch_host(host_problem: Problem, K: int, host_out, arena, stream=None):
     _check(lib.idx_launch_host(ctypes.byref(host_problem), int(K), _ptr(host_out), _ptr(arena),
                                arena.numel() * arena.element_size(), _stream(stream)),
@@ -256,6 +276,15 @@ class DeviceProblem:
             out = torch.empty((self.R, self.K), dtype=torch.int32, device=self.q.device)
         idx_launch(self.problem, self.K, out, self.ws, stream)
         return out
+
+    def launch_scored(self, out=None, out_score=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.R, self.K), dtype=torch.int32, device=self.q.device)
+        if out_score is None:
+            out_score = torch.empty((self.R, self.K), dtype=torch.float32, device=self.q.device)
+        idx_launch_scored(self.problem, self.K, out, out_score, self.ws, stream)
+        return out, out_score
 
     def status(self, stream=None) -> int:
         return last_device_status(self.ws, stream)

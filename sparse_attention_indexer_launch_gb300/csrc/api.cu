@@ -271,8 +271,9 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
   return cuda_ok(idx::launch_collect(a, s));
 }
 
-idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws, size_t ws_bytes,
-                      void *stream) {
+namespace {
+idx_status launch_impl(const idx_problem *problem, int32_t K, int32_t *out_idx, float *out_score, void *ws,
+                       size_t ws_bytes, void *stream) {
   idx_status st = check_problem(problem);
   if (st != IDX_OK) return st;
   if (out_idx == nullptr || ws == nullptr || K < 1 || K > IDX_MAX_K) return IDX_EINVAL;
@@ -290,6 +291,7 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   a.K = K;
   a.max_bound = problem->max_bound;
   a.out_idx = out_idx;
+  a.out_score = out_score;
   a.ws = w;
   a.bulk_rows = (reinterpret_cast<uintptr_t>(w.scores) & 15u) == 0 && w.scores_ld % 4 == 0;
   a.wait_limit_ns = wait_limit();
@@ -298,6 +300,43 @@ idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, v
   if (st != IDX_OK) return st;
   a.num_sms = sms;
   return cuda_ok(idx::launch_collect(a, s));
+}
+}  // namespace
+
+idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws, size_t ws_bytes,
+                      void *stream) {
+  return launch_impl(problem, K, out_idx, nullptr, ws, ws_bytes, stream);
+}
+
+idx_status idx_launch_scored(const idx_problem *problem, int32_t K, int32_t *out_idx, float *out_score, void *ws,
+                             size_t ws_bytes, void *stream) {
+  if (out_score == nullptr) return IDX_EINVAL;
+  return launch_impl(problem, K, out_idx, out_score, ws, ws_bytes, stream);
+}
+
+idx_status idx_merge_topk(const int32_t *part_idx, const float *part_score, const int32_t *part_offset,
+                          int32_t S, int32_t R, int32_t Kin, int32_t K, int32_t *out_idx, float *out_score,
+                          void *stream) {
+  if (part_idx == nullptr || part_score == nullptr || part_offset == nullptr || out_idx == nullptr)
+    return IDX_EINVAL;
+  if (S < 1 || R < 1 || Kin < 1 || K < 1 || K > IDX_MAX_K || Kin > IDX_MAX_K) return IDX_EINVAL;
+  if (S > IDX_MERGE_MAX_PARTS || R > IDX_MAX_ROWS) return IDX_EUNSUPPORTED;
+  if (idx::merge_smem_bytes(S, Kin, K) > idx::merge_smem_bytes(IDX_MERGE_MAX_PARTS, IDX_MAX_K, IDX_MAX_K))
+    return IDX_EUNSUPPORTED;
+  idx::MergeArgs m{};
+  for (int s = 0; s < S; ++s) {
+    if (part_offset[s] < 0) return IDX_EINVAL;
+    m.offset[s] = part_offset[s];
+  }
+  m.part_idx = part_idx;
+  m.part_score = part_score;
+  m.S = S;
+  m.R = R;
+  m.Kin = Kin;
+  m.K = K;
+  m.out_idx = out_idx;
+  m.out_score = out_score;
+  return cuda_ok(idx::launch_merge(m, static_cast<cudaStream_t>(stream)));
 }
 
 // ---------------------------------------------------------------------------- host inputs

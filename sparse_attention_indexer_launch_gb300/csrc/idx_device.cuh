@@ -375,4 +375,10 @@ __device__ __forceinline__ uint32_t radix_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose radix_key is k (inverse of radix_key; the key of -0.0 and +0.0
+// gives +0.0).
+__device__ __forceinline__ float radix_key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 }  // namespace idx

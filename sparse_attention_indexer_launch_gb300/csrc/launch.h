@@ -22,6 +22,7 @@ inline cudaError_t once_per_device(std::mutex &mu, bool (&done)[128], F setup) {
   if (done[dev]) return cudaSuccess;
   e = setup();
   if (e == cudaSuccess) done[dev] = true;
+  else (void)cudaGetLastError();   // a failed setup must not be reported again by a later launch
   return e;
 }
 
@@ -55,6 +56,7 @@ struct SelectArgs {
   const int32_t *bound;    // effective bounds [R]
   int32_t R, K, max_bound;
   int32_t *out_idx;        // [R][K]
+  float *out_score;        // [R][K] scores of the selected positions (-inf past them), or null
   Workspace ws;
   int32_t bulk_rows;       // scores and ld allow 16-byte bulk copies of row slices
   uint64_t wait_limit_ns;
@@ -92,6 +94,16 @@ struct PatchArgs {
   int64_t P;
 };
 
+constexpr int kMergeMaxParts = 8;
+struct MergeArgs {
+  const int32_t *part_idx;   // [S][R][Kin] positions within each part, descending order, -1 padded
+  const float *part_score;   // [S][R][Kin] their scores
+  int32_t offset[kMergeMaxParts];   // added to part s's positions
+  int32_t S, R, Kin, K;
+  int32_t *out_idx;          // [R][K]
+  float *out_score;          // [R][K] or null
+};
+
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
 cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
                          cudaStream_t stream);
@@ -102,6 +114,9 @@ cudaError_t launch_hist12(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_collect(const SelectArgs &a, cudaStream_t stream);
 // Every row's new key into the paged cache at position bound - 1.
 cudaError_t launch_patch(const PatchArgs &a, cudaStream_t stream);
+// Exact top-K of the union of S ranked parts (the key-sharded selection's merge).
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
+size_t merge_smem_bytes(int S, int Kin, int K);
 // Top-1 of each row of logits (one launch: splits and last-arriver finalize).
 cudaError_t launch_top1(const Top1Args &a, int num_sms, cudaStream_t stream);
 

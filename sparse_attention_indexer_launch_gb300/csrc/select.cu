@@ -62,6 +62,13 @@ __device__ __forceinline__ unsigned long long composite(uint32_t key, int64_t po
   return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
 }
 
+// The selection's output for slot j of a row: the position, and the score when the
+// caller asked for it (recovered exactly from the composite key's radix key).
+__device__ __forceinline__ void put(const SelectArgs &a, int64_t at, unsigned long long c) {
+  a.out_idx[at] = static_cast<int32_t>(~static_cast<uint32_t>(c & 0xFFFFFFFFull));
+  if (a.out_score != nullptr) a.out_score[at] = radix_key_value(static_cast<uint32_t>(c >> 32));
+}
+
 __device__ __forceinline__ int nslices(int32_t bound) { return bound > 0 ? (bound + kSlice - 1) / kSlice : 1; }
 
 // Block-wide exclusive scan of v (every thread must call).
@@ -687,7 +694,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
     __syncthreads();
     const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, static_cast<int>(nw), bstart, bcur, scratch);
     for (uint32_t i = tid; i < nw; i += kThreads)
-      out[i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
+      put(a, static_cast<int64_t>(r) * K + i, sorted[i]);
     return;
   }
 
@@ -702,7 +709,10 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   for (int i = tid; i < kSubBins; i += kThreads) hbuf[i] = __ldcg(&ws.hist_sub[static_cast<int64_t>(r) * kSubBins + i]);
   if (tid == 0) count_s = 0;
   const uint32_t need = static_cast<uint32_t>(nout) - above;
-  for (int j = nout + tid; j < K; j += kThreads) out[j] = -1;
+  for (int j = nout + tid; j < K; j += kThreads) {
+    out[j] = -1;
+    if (a.out_score != nullptr) a.out_score[static_cast<int64_t>(r) * K + j] = __uint_as_float(0xFF800000u);
+  }
   if (need == 0) return;
   if (nt <= static_cast<uint32_t>(kTieCap)) {
 #pragma unroll
@@ -776,7 +786,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
         const uint32_t g0 = bstart[sub], g1 = g0 + bcur[sub];
         uint32_t rank = 0u;
         for (uint32_t j = g0; j < g1; ++j) rank += sel[j] > x ? 1u : 0u;
-        out[above + g0 + rank] = static_cast<int32_t>(~static_cast<uint32_t>(x & 0xFFFFFFFFull));
+        put(a, static_cast<int64_t>(r) * K + above + g0 + rank, x);
       }
       return;
     }
@@ -810,7 +820,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   const int n = min(static_cast<int>(count_s), static_cast<int>(need));
   const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch);
   for (int i = tid; i < n; i += kThreads)
-    out[above + i] = static_cast<int32_t>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull));
+    put(a, static_cast<int64_t>(r) * K + above + i, sorted[i]);
 }
 
 }  // namespace

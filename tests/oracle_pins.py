@@ -471,6 +471,65 @@ def pin_patch_position(orc):
             assert moved <= set(expect), sorted(moved)
 
 
+def _split_topk(orc, scores, bounds, cuts, K):
+    """Each part [cuts[s], cuts[s+1]) of every row ranked on its own: positions in
+    the part's numbering and their scores, as a key-sharded indexer produces them."""
+    R = scores.shape[0]
+    S = len(cuts) - 1
+    pi = np.full((S, R, K), -1, np.int32)
+    ps = np.zeros((S, R, K), np.float32)
+    for si in range(S):
+        a, b = cuts[si], cuts[si + 1]
+        sub = np.ascontiguousarray(scores[:, a:b])
+        sb = np.clip(bounds - a, 0, b - a).astype(np.int32)
+        idx = orc.topk(sub, sb, K)
+        pi[si] = idx
+        for r in range(R):
+            ok = idx[r] >= 0
+            ps[si, r, ok] = sub[r, idx[r, ok]]
+    return pi, ps
+
+
+def pin_merge_equals_unsharded_topk(orc):
+    """The merge of the parts' own top-K lists equals the top-K of the whole rows
+    (a different path: oracle_topk over the scores), for 2, 3 and 8 parts, with
+    ties across part edges and rows whose bound is below K or inside a part."""
+    rng = np.random.default_rng(51)
+    R, L, K = 4, 3000, 256
+    scores = rng.integers(-40, 40, (R, L)).astype(np.float32)     # heavy ties
+    scores[1] = rng.standard_normal(L).astype(np.float32)
+    bounds = np.array([L, L - 17, 200, 1234], np.int32)
+    full = orc.topk(scores, bounds, K)
+    for cuts in ([0, 1500, L], [0, 64, 2000, L], list(np.linspace(0, L, 9).astype(int))):
+        pi, ps = _split_topk(orc, scores, bounds, cuts, K)
+        got = orc.merge_topk(pi, ps, np.array(cuts[:-1], np.int32), K)
+        assert np.array_equal(got, full), cuts
+
+
+def pin_merge_bruteforce(orc):
+    """Tiny random parts against Python's sorted over the union (score descending,
+    position ascending), including empty entries and equal scores."""
+    rng = np.random.default_rng(52)
+    for _ in range(30):
+        S, R, Kin, K = int(rng.integers(1, 5)), 2, int(rng.integers(1, 6)), int(rng.integers(1, 9))
+        offsets = np.cumsum(rng.integers(0, 20, S)).astype(np.int32)
+        pi = np.full((S, R, Kin), -1, np.int32)
+        ps = np.zeros((S, R, Kin), np.float32)
+        for s_ in range(S):
+            for r in range(R):
+                n = int(rng.integers(0, Kin + 1))
+                pos = rng.choice(20, size=n, replace=False)
+                pi[s_, r, :n] = pos
+                ps[s_, r, :n] = rng.integers(-3, 3, n)
+        got = orc.merge_topk(pi, ps, offsets, K)
+        for r in range(R):
+            pairs = [(float(ps[s_, r, j]), int(pi[s_, r, j]) + int(offsets[s_]))
+                     for s_ in range(S) for j in range(Kin) if pi[s_, r, j] >= 0]
+            want = [p for _, p in sorted(pairs, key=lambda t: (-t[0], t[1]))][:K]
+            want += [-1] * (K - len(want))
+            assert list(got[r]) == want, (got[r], want)
+
+
 ALL_PINS = [
     pin_e4m3_all_codes, pin_e4m3_closed_forms, pin_bf16_decode,
     pin_long_page_table, pin_page_table_scale_and_bound,
@@ -480,4 +539,5 @@ ALL_PINS = [
     pin_topk_padding, pin_radix_key_monotone, pin_radix_first_digit, pin_first_digit_hist,
     pin_top1_bruteforce, pin_top1_special_values,
     pin_e4m3_encode_vs_library, pin_e4m3_encode_roundtrip, pin_quantize_key, pin_patch_position,
+    pin_merge_equals_unsharded_topk, pin_merge_bruteforce,
 ]

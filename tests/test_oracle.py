@@ -57,6 +57,11 @@ MUTATIONS = [
     ("new_key_row_as_request", "page_table[(int64_t)row_req[r] * pt_stride + t / ORACLE_PAGE]",
      "page_table[(int64_t)r * pt_stride + t / ORACLE_PAGE]"),
     ("new_key_for_bound_zero", "    if (row_bound[r] == 0) return 0;\n", ""),
+    ("merge_offset_dropped", "v[n].pos = part_idx[at] + offset[s];", "v[n].pos = part_idx[at];"),
+    ("merge_empty_entries_kept", "if (part_idx[at] < 0) continue;", ""),
+    ("merge_no_padding", "out_idx[(int64_t)r * K + j] = j < n ? v[j].pos : -1;",
+     "out_idx[(int64_t)r * K + j] = j < n ? v[j].pos : 0;"),
+    ("merge_part_stride", "const int64_t at = ((int64_t)s * R + r) * Kin + j;", "const int64_t at = ((int64_t)r * S + s) * Kin + j;"),
 ]
 
 
