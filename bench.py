@@ -341,8 +341,31 @@ def run_patch(args):
         b.record(stream)
     torch.cuda.synchronize()
     us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    # the launch with and without the new keys written by its own first kernel,
+    # against the patch launch followed by the plain launch (L2 flushed before each)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    us_fused = timed(lambda: lib.idx_launch_new_keys(dp.problem, k_new, prob.K, out, dp.ws))
+    us_split = timed(lambda: (lib.idx_patch_new_keys(dp.problem, k_new), dp.launch(out)))
+    us_plain = timed(lambda: dp.launch(out))
     print(json.dumps({"metric": "µs per new-key patch (8 rows, E4M3 cache), CUDA-graph replay", "op": "patch",
                       "value": us, "us_per_call_from_python": us_call,
+                      "launch_with_new_keys_us": us_fused, "patch_then_launch_us": us_split,
+                      "launch_alone_us": us_plain,
                       "unit": "µs", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
                       "warmup": args.warmup, "config": {"workload": workloads.CONFIG_NAMES[3]}}))
     return 0

@@ -212,6 +212,19 @@ void idx_profile_events(void *start, void *stop);
  * its own position).  Asynchronous on `stream`; allocates nothing. */
 idx_status idx_patch_new_keys(const idx_problem *problem, const void *k_new, void *stream);
 
+/* idx_launch with the rows' new keys written first, inside the launch (the same
+ * page section, "New keys": a key the launch writes is scored by every row of its
+ * request whose bound covers it).  The launch's first kernel writes row r's key
+ * at position row_bound[r] - 1 exactly as idx_patch_new_keys does, before the
+ * scan reads the cache; the result equals idx_patch_new_keys followed by
+ * idx_launch, in one launch sequence instead of two.
+ *   problem  as for idx_launch; problem->k_cache and problem->k_scale are WRITTEN.
+ *   k_new    device bf16 [R][128], 16-byte aligned (NULL or misaligned: IDX_EINVAL).
+ * Other arguments, outputs and errors as for idx_launch; rows of one request must
+ * have different bounds. */
+idx_status idx_launch_new_keys(const idx_problem *problem, const void *k_new, int32_t K, int32_t *out_idx,
+                               void *ws, size_t ws_bytes, void *stream);
+
 /* Top-1 of each row of logits in one launch: the later "draft_topk1_postprocess"
  * commit on the sglang PR 48224 page.  Each split of a row folds its (value,
  * lowest index) into a per-row 64-bit key with an atomic maximum; the split that

@@ -27,7 +27,7 @@ IDX_DEBUG_WAIT_LIMIT_NS, IDX_DEBUG_STALL_SCORE_MMA = 1, 2
 EXPORTS = ["idx_workspace_size", "idx_score", "idx_topk", "idx_launch", "idx_host_arena_size",
            "idx_launch_host", "idx_last_device_status", "idx_status_string", "idx_version",
            "idx_debug_set", "idx_profile_events", "idx_top1_state_size", "idx_top1", "idx_topk_noalloc",
-           "idx_patch_new_keys", "idx_launch_scored", "idx_merge_topk"]
+           "idx_patch_new_keys", "idx_launch_scored", "idx_merge_topk", "idx_launch_new_keys"]
 
 
 class IdxError(RuntimeError):
@@ -88,6 +88,8 @@ def _load():
     lib.idx_launch_scored.restype = ctypes.c_int
     lib.idx_merge_topk.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), i32, i32, i32, i32, vp, vp, vp]
     lib.idx_merge_topk.restype = ctypes.c_int
+    lib.idx_launch_new_keys.argtypes = [P, vp, i32, vp, vp, sz, vp]
+    lib.idx_launch_new_keys.restype = ctypes.c_int
     return lib
 
 
@@ -176,6 +178,13 @@ def idx_topk_noalloc(scores, ld: int, row_bound, R: int, max_bound: int, K: int,
 def idx_launch(problem: Problem, K: int, out_idx, ws, stream=None):
     _check(lib.idx_launch(ctypes.byref(problem), int(K), _ptr(out_idx), _ptr(ws),
                           ws.numel() * ws.element_size(), _stream(stream)), "idx_launch")
+
+
+def idx_launch_new_keys(problem: Problem, k_new, K: int, out_idx, ws, stream=None):
+    """idx_launch with every row's new key (bf16 [R][128] device tensor) written
+    into the problem's cache first, inside the launch (see idx.h)."""
+    _check(lib.idx_launch_new_keys(ctypes.byref(problem), _ptr(k_new), int(K), _ptr(out_idx), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)), "idx_launch_new_keys")
 
 
 def idx_launch_scored(problem: Problem, K: int, out_idx, out_score, ws, stream=None):

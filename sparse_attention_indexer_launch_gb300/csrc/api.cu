@@ -159,8 +159,25 @@ idx_status key_tensor_map(const idx_problem *p, CUtensorMap *map) {
 idx_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? IDX_OK : IDX_ECUDA; }
 
 // prep + scoring launches shared by idx_score and idx_launch.
+// The new-key writes of a problem's rows (k_new: bf16 [R][128], device).
+idx::PatchArgs make_patch(const idx_problem *problem, const void *k_new) {
+  idx::PatchArgs pa{};
+  pa.k_new = static_cast<const uint16_t *>(k_new);
+  pa.row_req = problem->row_req;
+  pa.row_bound = problem->row_bound;
+  pa.page_table = problem->page_table;
+  pa.k_cache = const_cast<void *>(problem->k_cache);
+  pa.k_scale = const_cast<float *>(problem->k_scale);
+  pa.R = problem->R;
+  pa.Q = problem->Q;
+  pa.pt_stride = problem->pt_stride;
+  pa.kv_dtype = problem->kv_dtype;
+  pa.P = problem->P;
+  return pa;
+}
+
 idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, int64_t ld, uint32_t *hist,
-                       bool clear_select, cudaStream_t s) {
+                       bool clear_select, const void *k_new, cudaStream_t s) {
   int sms = 0;
   idx_status st = device_sms(&sms);
   if (st != IDX_OK) return st;
@@ -180,6 +197,7 @@ idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, 
   pa.hist_target = hist;
   pa.clear_select = clear_select ? 1 : 0;
   pa.ws = w;
+  if (k_new != nullptr) pa.patch = make_patch(p, k_new);
   st = cuda_ok(idx::launch_prep(pa, s));
   if (st != IDX_OK) return st;
   idx::ScoreArgs sa{};
@@ -235,7 +253,7 @@ idx_status idx_score(const idx_problem *problem, float *scores, int64_t ld, uint
   const Layout L = make_layout(problem->R, 1, problem->max_bound, false);
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
   const Workspace w = carve(ws, L);
-  return run_scoring(problem, w, scores, ld, hist, false, static_cast<cudaStream_t>(stream));
+  return run_scoring(problem, w, scores, ld, hist, false, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, int32_t R, int32_t max_bound,
@@ -272,8 +290,8 @@ idx_status idx_topk(const float *scores, int64_t ld, const int32_t *row_bound, i
 }
 
 namespace {
-idx_status launch_impl(const idx_problem *problem, int32_t K, int32_t *out_idx, float *out_score, void *ws,
-                       size_t ws_bytes, void *stream) {
+idx_status launch_impl(const idx_problem *problem, const void *k_new, int32_t K, int32_t *out_idx, float *out_score,
+                       void *ws, size_t ws_bytes, void *stream) {
   idx_status st = check_problem(problem);
   if (st != IDX_OK) return st;
   if (out_idx == nullptr || ws == nullptr || K < 1 || K > IDX_MAX_K) return IDX_EINVAL;
@@ -281,7 +299,7 @@ idx_status launch_impl(const idx_problem *problem, int32_t K, int32_t *out_idx, 
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return IDX_EINVAL;
   const Workspace w = carve(ws, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_scoring(problem, w, w.scores, w.scores_ld, nullptr, true, s);
+  st = run_scoring(problem, w, w.scores, w.scores_ld, nullptr, true, k_new, s);
   if (st != IDX_OK) return st;
   idx::SelectArgs a{};
   a.scores = w.scores;
@@ -305,13 +323,19 @@ idx_status launch_impl(const idx_problem *problem, int32_t K, int32_t *out_idx, 
 
 idx_status idx_launch(const idx_problem *problem, int32_t K, int32_t *out_idx, void *ws, size_t ws_bytes,
                       void *stream) {
-  return launch_impl(problem, K, out_idx, nullptr, ws, ws_bytes, stream);
+  return launch_impl(problem, nullptr, K, out_idx, nullptr, ws, ws_bytes, stream);
+}
+
+idx_status idx_launch_new_keys(const idx_problem *problem, const void *k_new, int32_t K, int32_t *out_idx, void *ws,
+                               size_t ws_bytes, void *stream) {
+  if (k_new == nullptr || (reinterpret_cast<uintptr_t>(k_new) & 15u) != 0) return IDX_EINVAL;
+  return launch_impl(problem, k_new, K, out_idx, nullptr, ws, ws_bytes, stream);
 }
 
 idx_status idx_launch_scored(const idx_problem *problem, int32_t K, int32_t *out_idx, float *out_score, void *ws,
                              size_t ws_bytes, void *stream) {
   if (out_score == nullptr) return IDX_EINVAL;
-  return launch_impl(problem, K, out_idx, out_score, ws, ws_bytes, stream);
+  return launch_impl(problem, nullptr, K, out_idx, out_score, ws, ws_bytes, stream);
 }
 
 idx_status idx_merge_topk(const int32_t *part_idx, const float *part_score, const int32_t *part_offset,
@@ -465,19 +489,7 @@ idx_status idx_patch_new_keys(const idx_problem *problem, const void *k_new, voi
   idx_status st = check_problem(problem);
   if (st != IDX_OK) return st;
   if (k_new == nullptr || (reinterpret_cast<uintptr_t>(k_new) & 15u) != 0) return IDX_EINVAL;
-  idx::PatchArgs pa{};
-  pa.k_new = static_cast<const uint16_t *>(k_new);
-  pa.row_req = problem->row_req;
-  pa.row_bound = problem->row_bound;
-  pa.page_table = problem->page_table;
-  pa.k_cache = const_cast<void *>(problem->k_cache);
-  pa.k_scale = const_cast<float *>(problem->k_scale);
-  pa.R = problem->R;
-  pa.Q = problem->Q;
-  pa.pt_stride = problem->pt_stride;
-  pa.kv_dtype = problem->kv_dtype;
-  pa.P = problem->P;
-  return cuda_ok(idx::launch_patch(pa, static_cast<cudaStream_t>(stream)));
+  return cuda_ok(idx::launch_patch(make_patch(problem, k_new), static_cast<cudaStream_t>(stream)));
 }
 
 size_t idx_top1_state_size(int32_t R) {

@@ -26,6 +26,15 @@ inline cudaError_t once_per_device(std::mutex &mu, bool (&done)[128], F setup) {
   return e;
 }
 
+struct PatchArgs {
+  const uint16_t *k_new;   // bf16 [R][128]
+  const int32_t *row_req, *row_bound, *page_table;
+  void *k_cache;           // E4M3 bytes or bf16 [P][64][128]
+  float *k_scale;          // [P][64] for E4M3
+  int32_t R, Q, pt_stride, kv_dtype;
+  int64_t P;
+};
+
 struct PrepArgs {
   const void *q;
   const float *w;
@@ -35,6 +44,7 @@ struct PrepArgs {
   uint32_t *hist_target;   // first-digit histogram the scoring kernel will fill (cleared here), or null
   int32_t clear_select;    // also clear the selection state (rowsel)
   Workspace ws;
+  PatchArgs patch;         // rows' new keys written into the cache first (patch.k_new null: none)
 };
 
 struct ScoreArgs {
@@ -85,14 +95,6 @@ struct Top1Args {
   int32_t vec4;            // rows and chunks allow 16-byte loads
 };
 
-struct PatchArgs {
-  const uint16_t *k_new;   // bf16 [R][128]
-  const int32_t *row_req, *row_bound, *page_table;
-  void *k_cache;           // E4M3 bytes or bf16 [P][64][128]
-  float *k_scale;          // [P][64] for E4M3
-  int32_t R, Q, pt_stride, kv_dtype;
-  int64_t P;
-};
 
 constexpr int kMergeMaxParts = 8;
 struct MergeArgs {

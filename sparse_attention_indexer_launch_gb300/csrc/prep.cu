@@ -10,6 +10,7 @@
 
 #include "idx_device.cuh"
 #include "launch.h"
+#include "new_key.cuh"
 
 namespace idx {
 namespace {
@@ -265,6 +266,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   if (blockIdx.x == a.R) {
     plan_block(a);
   } else {
+    // the row's new key first (the fused new-key launch): the scan that follows
+    // this launch reads the cache only after the whole grid has finished
+    if (a.patch.k_new != nullptr && threadIdx.x < 32) store_new_key(a.patch, blockIdx.x, threadIdx.x);
     prep_row(a, blockIdx.x);
     clear_row_state(a, blockIdx.x);
   }

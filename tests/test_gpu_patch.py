@@ -68,3 +68,26 @@ def test_patch_of_a_large_batch_matches_the_oracle(lib, orc):
     torch.cuda.synchronize()
     assert np.array_equal(dp.k_cache.cpu().numpy(), ref.k_cache)
     assert np.array_equal(dp.k_scale.cpu().numpy().view(np.uint32), ref.k_scale.view(np.uint32))
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "bf16"])
+def test_launch_with_new_keys_equals_patch_then_launch(lib, orc, kv):
+    """idx_launch_new_keys (the keys written by the launch's own first kernel)
+    leaves the same cache as the oracle's patch and selects exactly what
+    idx_patch_new_keys followed by idx_launch selects."""
+    prob = workloads.build("fused_patch", [3000, 64, 129, 5000], [4, 1, 2, 3], kv, seed=45,
+                           bounds=[[2997, 2998, 2999, 3000], [64], [0, 129], [4031, 4032, 4033]])
+    k_new = torch.from_numpy(_new_keys(46, prob.R, scale=2.0).view(np.int16)).cuda()
+    ref = orc.patch_new_keys(prob, k_new.cpu().numpy().view(np.uint16))
+    fused = lib.DeviceProblem(prob)
+    out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
+    lib.idx_launch_new_keys(fused.problem, k_new, prob.K, out, fused.ws)
+    assert fused.status() == lib.IDX_OK
+    if kv == "e4m3":
+        assert np.array_equal(fused.k_cache.cpu().numpy(), ref.k_cache)
+        assert np.array_equal(fused.k_scale.cpu().numpy().view(np.uint32), ref.k_scale.view(np.uint32))
+    else:
+        assert np.array_equal(fused.k_cache.view(torch.int16).cpu().numpy().view(np.uint16), ref.k_cache)
+    split = lib.DeviceProblem(prob)
+    lib.idx_patch_new_keys(split.problem, k_new)
+    assert np.array_equal(out.cpu().numpy(), split.launch().cpu().numpy())
