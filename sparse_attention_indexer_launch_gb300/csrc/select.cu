@@ -514,12 +514,13 @@ __device__ __forceinline__ int sort_size(int n);
 // to 12 bits (the span's top 12 significant bits), give 4096 buckets; a counting
 // pass places each bucket's keys in a contiguous group, and each key's rank
 // among the members of its group (all 64 bits compared) gives its final slot.
-// When some group holds more than kGroupMax keys (many equal or near-equal
-// scores) the segment is sorted by block_sort_desc instead.  tmp[] (kSortCap keys)
+// A key's rank costs one compare per member of its group, so groups of up to
+// kGroupMax keys are ranked this way; when some group holds more (many equal or
+// near-equal scores) the segment is sorted by block_sort_desc instead.  tmp[] (kSortCap keys)
 // and start[], cur[] (4096 words each) are scratch.  Returns the buffer holding
 // the result.  Every thread of the block must call.
 constexpr int kBuckets = 4096;
-constexpr int kGroupMax = 64;
+constexpr int kGroupMax = 256;
 
 __device__ unsigned long long *block_bucket_sort_desc(unsigned long long *s, unsigned long long *tmp, int n,
                                                       uint32_t *start, uint32_t *cur, uint32_t *scratch) {
