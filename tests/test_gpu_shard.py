@@ -73,3 +73,49 @@ def test_merge_rejects_bad_arguments(lib):
     with pytest.raises(lib.IdxError) as e:
         lib.idx_merge_topk(pi[:2], ps[:2], [0, -64], 16, out)   # negative offset
     assert e.value.status == lib.IDX_EINVAL
+
+
+def _ranked_parts(orc, scores, bounds, cuts, Kin):
+    """Each part [cuts[s], cuts[s+1]) of every row ranked on its own by the oracle:
+    positions in the part's numbering (-1 padded) and their scores."""
+    R = scores.shape[0]
+    S = len(cuts) - 1
+    pi = np.full((S, R, Kin), -1, np.int32)
+    ps = np.zeros((S, R, Kin), np.float32)
+    for s in range(S):
+        a, b = cuts[s], cuts[s + 1]
+        sub = np.ascontiguousarray(scores[:, a:b])
+        idx = orc.topk(sub, np.clip(bounds - a, 0, b - a).astype(np.int32), Kin)
+        pi[s] = idx
+        for r in range(R):
+            ok = idx[r] >= 0
+            ps[s, r, ok] = sub[r, idx[r, ok]]
+    return pi, ps
+
+
+@pytest.mark.parametrize("Kin,K", [(64, 64), (64, 100), (300, 32), (2048, 2048)])
+def test_merge_matches_the_oracle_on_crafted_lists(lib, orc, Kin, K):
+    """Integer scores (ties within and across parts, -0.0 against +0.0), a part
+    that holds no key of some rows, parts shorter than Kin, and K above or below
+    the lists' length; compared with the oracle's merge of the same lists,
+    positions and scores."""
+    rng = np.random.default_rng(71 + Kin + K)
+    R, L = 6, 5000
+    scores = rng.integers(-6, 6, (R, L)).astype(np.float32)
+    scores[scores == 0] = -0.0
+    scores[0, ::3] = 0.0
+    scores[1] = rng.standard_normal(L).astype(np.float32)
+    bounds = np.array([L, 40, 0, 1300, L - 3, 2001], np.int32)    # row 1: only the first part
+    cuts = [0, 1000, 1003, 2000, L]                                # a 3-key part
+    pi, ps = _ranked_parts(orc, scores, bounds, cuts, Kin)
+    want = orc.merge_topk(pi, ps, np.array(cuts[:-1], np.int32), K)
+    out = torch.full((R, K), -7, dtype=torch.int32, device="cuda")
+    out_s = torch.full((R, K), 7.0, dtype=torch.float32, device="cuda")
+    lib.idx_merge_topk(torch.from_numpy(pi).cuda(), torch.from_numpy(ps).cuda(), cuts[:-1], K, out, out_s)
+    got, got_s = out.cpu().numpy(), out_s.cpu().numpy()
+    assert np.array_equal(got, want)
+    for r in range(R):
+        n = int((got[r] >= 0).sum())
+        assert np.array_equal(got_s[r, :n], scores[r, got[r, :n]]), r
+        assert np.all(np.isneginf(got_s[r, n:])), r
+    assert (got[2] == -1).all()                                    # bound 0: all padding
