@@ -83,6 +83,12 @@ typedef struct {
     int32_t max_bound;         /* host upper bound on every row_bound[r]; sizes scratch, so no
                                   device-to-host read is needed; 0 <= max_bound <= pt_stride*64 */
     int32_t kv_dtype;          /* idx_kv_dtype */
+    int32_t rows_hint;         /* host hint, like max_bound: 0 if unknown, else an upper bound on the
+                                  rows of any one request in this problem.  1 or 2 (a lone live row,
+                                  or a row and its pad row) lets the scan batch 4 / rows tiles into
+                                  one accumulator so that every epilogue warp has work.  The result
+                                  never depends on it: a hint below the true count only costs
+                                  speed.  Negative: IDX_EINVAL. */
 } idx_problem;
 
 /* Bytes of device workspace that idx_score / idx_topk / idx_launch need for this

@@ -43,7 +43,7 @@ class Problem(ctypes.Structure):
         ("k_scale", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("row_req", ctypes.c_void_p),
         ("row_bound", ctypes.c_void_p), ("R", ctypes.c_int32), ("Q", ctypes.c_int32),
         ("P", ctypes.c_int64), ("pt_stride", ctypes.c_int32), ("max_bound", ctypes.c_int32),
-        ("kv_dtype", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("rows_hint", ctypes.c_int32),
     ]
 
 
@@ -116,16 +116,18 @@ def _stream(stream):
 
 
 def make_problem(q, w, k_cache, k_scale, page_table, row_req, row_bound, max_bound: int,
-                 kv_dtype: int, P: int | None = None) -> Problem:
+                 kv_dtype: int, P: int | None = None, rows_hint: int = 0) -> Problem:
     """idx_problem from tensors (device tensors for the device calls, host tensors
     for idx_launch_host).  Shapes: q [R][64][128] bf16, w [R][64] fp32, k_cache
     [P][64][128] uint8 (E4M3 bytes) or bf16, k_scale [P][64] fp32 or None,
-    page_table [Q][stride] int32, row_req and row_bound [R] int32."""
+    page_table [Q][stride] int32, row_req and row_bound [R] int32.  rows_hint: the
+    most rows any request has (0: unknown)."""
     R = int(row_bound.shape[0])
     return Problem(q=_ptr(q), w=_ptr(w), k_cache=_ptr(k_cache), k_scale=_ptr(k_scale),
                    page_table=_ptr(page_table), row_req=_ptr(row_req), row_bound=_ptr(row_bound),
                    R=R, Q=int(page_table.shape[0]), P=int(P if P is not None else k_cache.shape[0]),
-                   pt_stride=int(page_table.shape[1]), max_bound=int(max_bound), kv_dtype=int(kv_dtype))
+                   pt_stride=int(page_table.shape[1]), max_bound=int(max_bound), kv_dtype=int(kv_dtype),
+                   rows_hint=int(rows_hint))
 
 
 def workspace_size(problem: Problem, K: int) -> int:
@@ -237,7 +239,10 @@ class DeviceProblem:
     """A workloads.Problem uploaded to the GPU (plain tensor copies), with its
     idx_problem and a workspace."""
 
-    def __init__(self, prob, device="cuda", K: int | None = None, max_bound: int | None = None):
+    def __init__(self, prob, device="cuda", K: int | None = None, max_bound: int | None = None,
+                 rows_hint: int | None = None):
+        """rows_hint: idx_problem.rows_hint; None counts the rows of each request
+        in the host problem's row map."""
         import numpy as np
         import torch
         self.host = prob
@@ -257,8 +262,12 @@ class DeviceProblem:
         self.row_req = torch.from_numpy(prob.row_req).to(dev)
         self.row_bound = torch.from_numpy(prob.row_bound).to(dev)
         self.max_bound = int(max_bound if max_bound is not None else max(prob.max_bound, 0))
+        if rows_hint is None:
+            req = np.asarray(prob.row_req)
+            rows_hint = int(np.bincount(req[req >= 0]).max()) if (req >= 0).any() else 0
         self.problem = make_problem(self.q, self.w, self.k_cache, self.k_scale, self.page_table,
-                                    self.row_req, self.row_bound, self.max_bound, self.kv, P=prob.P)
+                                    self.row_req, self.row_bound, self.max_bound, self.kv, P=prob.P,
+                                    rows_hint=rows_hint)
         self.ws = alloc_bytes(workspace_size(self.problem, self.K), dev)
         self.R = prob.R
 

@@ -93,7 +93,8 @@ idx_status check_problem(const idx_problem *p) {
   if (p->q == nullptr || p->w == nullptr || p->k_cache == nullptr || p->page_table == nullptr ||
       p->row_req == nullptr || p->row_bound == nullptr)
     return IDX_EINVAL;
-  if (p->R < 1 || p->Q < 1 || p->P < 1 || p->pt_stride < 1 || p->max_bound < 0) return IDX_EINVAL;
+  if (p->R < 1 || p->Q < 1 || p->P < 1 || p->pt_stride < 1 || p->max_bound < 0 || p->rows_hint < 0)
+    return IDX_EINVAL;
   if (p->R > IDX_MAX_ROWS) return IDX_EUNSUPPORTED;
   if (static_cast<int64_t>(p->max_bound) > static_cast<int64_t>(p->pt_stride) * IDX_PAGE) return IDX_EINVAL;
   if (p->P > (INT32_MAX / IDX_PAGE)) return IDX_EUNSUPPORTED;  // TMA row coordinate is 32-bit
@@ -220,7 +221,7 @@ idx_status run_scoring(const idx_problem *p, const Workspace &w, float *scores, 
     g_prof_start = g_prof_stop = nullptr;
   }
   if (ev0 != nullptr && cudaEventRecord(ev0, s) != cudaSuccess) return IDX_ECUDA;
-  st = cuda_ok(idx::launch_score(map, sa, p->kv_dtype, sms, s));
+  st = cuda_ok(idx::launch_score(map, sa, p->kv_dtype, p->rows_hint == 1 || p->rows_hint == 2, sms, s));
   if (st != IDX_OK) return st;
   if (ev1 != nullptr && cudaEventRecord(ev1, s) != cudaSuccess) return IDX_ECUDA;
   return IDX_OK;

@@ -107,7 +107,7 @@ struct MergeArgs {
 };
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t stream);
-cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
+cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, bool batched, int num_ctas,
                          cudaStream_t stream);
 // Selection.  idx_topk: clear the state and copy the bounds, build the 12-bit
 // histogram of the given scores.  Both paths end in the collect and finish launches.

@@ -55,6 +55,15 @@ constexpr int kHistWords = kHistBins / 2;   // two 16-bit counters per word
 constexpr int kFlushTiles = 256;            // 256 tiles x 128 keys < 65536: no counter overflows
 constexpr int kStageBlocks = 4;             // histogram blocks each epilogue warp has in flight to global
 
+// Groups of one or two rows leave most of an accumulator's 256 columns and most
+// epilogue warps idle.  The batched instance of the kernel (chosen by the host
+// when the caller says that no request has more than two rows) puts the CTA's
+// tiles into the accumulators in batches instead: 4 / rows consecutive tiles of
+// one group share one accumulator (N = 64 x rows each) and each epilogue warp
+// reduces one (tile, row) of a batch.  Groups of three or four rows still run
+// one tile per batch there, so the batched instance is exact for any rows.
+__device__ __forceinline__ int batch_tiles(int nrows) { return nrows <= 2 ? 4 / nrows : 1; }
+
 template <int KV>
 struct Cfg {
   static constexpr int kStageBytes = KV == IDX_KV_E4M3 ? kTileKeys * kDim : kTileKeys * kDim * 2;
@@ -185,7 +194,7 @@ __device__ __forceinline__ float reduce_quad(const float (&s)[4], int lane) {
   return k;
 }
 
-template <int KV>
+template <int KV, bool kBatched>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const ScoreArgs a) {
   using C = Cfg<KV>;
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       mbar_init(&bars->sempty[s], kEpiWarps);   // every epilogue warp passes every tile
     }
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&bars->tfull[s], 1);
+      mbar_init(&bars->tfull[s], kBatched ? kIssuers<KV> : 1);   // batched: every issuer commits every batch
       mbar_init(&bars->tempty[s], kEpiWarps);   // every epilogue warp reads every tile
     }
     mbar_init(&bars->hdone[0], kEpiWarps);
@@ -431,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       bool ok = true;
       GroupCursor cur;
       cur.seek(ws.groups, num_groups, T0);
+      uint32_t bn = 0;        // batched walk: batches of the CTA's sequence so far
       for (int g = cur.g; ok && g < num_groups; ++g) {
         const int gbeg = ws.groups[g].tile_begin;
         if (gbeg >= T1) break;
@@ -441,6 +451,57 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           break;
         }
         ++nswitch;
+        if constexpr (kBatched) {
+          // Batch b (batch_tiles(rows) consecutive tiles of the group) accumulates
+          // into slot b % 2, tile i of the batch at columns i x 64 x rows; both
+          // issuers walk every batch, wait for its slot, issue their own tiles of it
+          // (possibly none) and commit the slot, whose barrier counts both commits.
+          const int nrows = ws.groups[g].nrows;
+          const int bt = batch_tiles(nrows);
+          const uint32_t idesc_b = umma_idesc(fmt, 64u * static_cast<uint32_t>(nrows));
+          const int tbeg = gbeg > T0 ? gbeg : T0, tend = gend < T1 ? gend : T1;
+          for (int bs = tbeg; ok && bs < tend; bs += bt, ++bn) {
+            const uint32_t slot = bn % kSlots;
+            if (!mbar_wait(&bars->tempty[slot], ((bn / kSlots) & 1u) ^ 1u, limit, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int be = bs + bt < tend ? bs + bt : tend;
+            for (int tt = bs; tt < be; ++tt) {
+              if (nis == 2 && ((tt - T0) & 1) != par) continue;   // the other issuer's tile
+              if (!mbar_wait(&bars->full[s], sphase, limit, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d = tmem_base + slot * kSlotCols + static_cast<uint32_t>((tt - bs) * 64 * nrows);
+              const uint64_t adesc = adesc0 + static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t koff = (kk & 3) * 32;
+                const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + (koff >> 4);
+                if (KV == IDX_KV_E4M3) {
+                  umma_f8(d, adesc + (koff >> 4), bd, idesc_b, kk > 0);
+                } else {
+                  umma_f16(d, adesc + (((kk < 4 ? 0u : static_cast<uint32_t>(kTileKeys) * 128u) + koff) >> 4), bd,
+                           idesc_b, kk > 0);
+                }
+              }
+              umma_commit(&bars->empty[s]);
+              s += nis;
+              if (s >= C::kStages) {
+                s -= C::kStages;
+                sphase ^= 1u;
+              }
+            }
+            if (ok && !(a.stall_first_handoff && bn == 0)) umma_commit(&bars->tfull[slot]);
+          }
+          if (ok) umma_commit(&bars->bfree);
+          continue;
+        } else {
+          (void)bn;
+        }
         const uint32_t idesc = umma_idesc(fmt, 64u * static_cast<uint32_t>(ws.groups[g].nrows));
         const int tend = gend < T1 ? gend : T1;
         for (; t < tend; t += nis) {
@@ -588,6 +649,122 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       const int periodic = gbegin + ((t - gbegin) / kFlushTiles + 1) * kFlushTiles;
       next_fp = periodic < cur.next_begin ? periodic : cur.next_begin;
     };
+    if constexpr (kBatched) {
+      // The batched walk: warp q of a TMEM lane quarter (q = 0..3) reduces one
+      // (tile, row) of each batch: tile q with one row, row q % 2 of tile q / 2
+      // with two, row q of the batch's one tile with three or four.  The histogram
+      // goes to global memory before each group after the first, every
+      // kFlushTiles tiles within a group and at the end; every warp takes each of
+      // these points, in order.
+      const int rq = ew >> 2;   // this warp's rank among its quarter's four
+      const uint32_t tqb = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      int brow = 0, bi = 0, bt = 1;
+      int cnt = 1;              // this warp's share of the kEpiWarps arrivals on a tile's scale slot
+      uint32_t *bhrow = shist;
+      uint32_t bn = 0;          // batches of the CTA's sequence so far
+      bool first_group = true;
+      for (int g = cur.g; ok && g < num_groups; ++g) {
+        const int gbeg = ws.groups[g].tile_begin;
+        if (gbeg >= T1) break;
+        const int gend = g + 1 < num_groups ? ws.groups[g + 1].tile_begin : total_tiles;
+        if (gend <= gbeg) continue;
+        if (!first_group && !flush()) {
+          ok = false;
+          break;
+        }
+        first_group = false;
+        grp = ws.groups[g];
+        {
+          const int n = grp.nrows;
+          bt = batch_tiles(n);
+          brow = n >= 3 ? rq : (n == 2 ? (rq & 1) : 0);
+          bi = n >= 3 ? 0 : (n == 2 ? (rq >> 1) : rq);
+          mine = brow < n;
+          // readers of a tile per quarter: four (four rows), three (three: the first
+          // arrives twice), two (two rows) or one (one row); four arrivals in all
+          cnt = n == 4 ? 1 : n == 3 ? (brow == 0 ? 2 : 1) : n == 2 ? 2 : 4;
+          const int r = grp.row0 + (mine ? brow : 0);
+          bnd = mine ? ws.bound_eff[r] : 0;
+          gbegin = grp.tile_begin;
+          srow = a.scores + static_cast<int64_t>(r) * a.ld;
+          bhrow = shist + brow * kHistWords;
+          const float2 *wr = reinterpret_cast<const float2 *>(ws.wq + static_cast<int64_t>(r) * kHeads);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) w2[k] = wr[4 * k + (lane & 3)];
+        }
+        const int tbeg = gbeg > T0 ? gbeg : T0, tend = gend < T1 ? gend : T1;
+        int since = 0;   // tiles counted since the last flush
+        for (int bs = tbeg; bs < tend; bs += bt, ++bn) {
+          if (since + bt > kFlushTiles) {
+            if (!flush()) {
+              ok = false;
+              break;
+            }
+            since = 0;
+          }
+          since += bt;
+          const int t = bs + bi;
+          const bool act = mine && t < tend && bi < bt;
+          float scale = 1.0f;
+          if (KV == IDX_KV_E4M3 && act) {
+            const int k = t - T0;
+            const int ss = k & (kScaleSlots - 1);
+            if (!mbar_wait(&bars->sfull[ss], (k / kScaleSlots) & 1, limit, abort)) {
+              set_abort(bars, ws.status);
+              ok = false;
+              break;
+            }
+            scale = sc[ss * kTileKeys];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cnt(&bars->sempty[ss], static_cast<uint32_t>(cnt));
+          }
+          const uint32_t slot = bn % kSlots;
+          if (!mbar_wait(&bars->tfull[slot], (bn / kSlots) & 1u, limit, abort)) {
+            set_abort(bars, ws.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!act) {   // nothing of this batch for this warp: hand the accumulator back at once
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+            continue;
+          }
+          const int pos = (t - gbegin) * kTileKeys + qk;
+          const bool keep = pos < bnd;
+          const uint32_t negmask = __ballot_sync(0xffffffffu, keep && scale < 0.0f);
+          const uint32_t taddr = tqb + slot * kSlotCols + static_cast<uint32_t>((bi * grp.nrows + brow) * 64);
+          float2 sums[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t va[16], vb[16];
+            tmem_ld16x256_x4(taddr + half * 32, va);
+            tmem_ld16x256_x4(taddr + (16u << 16) + half * 32, vb);
+            tmem_wait_ld();
+            reg_fence16(va);
+            reg_fence16(vb);
+            if (half == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+            }
+            if (negmask == 0u) relu_frag(va, vb, &w2[4 * half], sums);
+            else relu_frag_signed(va, vb, &w2[4 * half], (negmask >> (lane & ~3)) & 15u, sums);
+          }
+          const float part[4] = {sums[0].x + sums[0].y, sums[1].x + sums[1].y, sums[2].x + sums[2].y,
+                                 sums[3].x + sums[3].y};
+          const float score = reduce_quad(part, lane) * scale;
+          if (keep) {
+            srow[pos] = score;
+            const uint32_t bin = radix_key(score) >> (32 - kHistBits);
+            atomicAdd(&bhrow[bin >> 1], 1u << ((bin & 1) * 16));
+          }
+        }
+      }
+      if (ok) flush();
+    } else {
     load_group();
     set_next_fp(T0);
 
@@ -661,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       }
     }
     if (ok) flush();
+    }
   }
 
   // Every role is done (or gave up); release TMEM.
@@ -672,13 +850,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
 }
 
-template <int KV>
+template <int KV, bool kBatched>
 cudaError_t launch_kv(const CUtensorMap &kmap, const ScoreArgs &a, int num_ctas, cudaStream_t stream) {
   static std::mutex mu;
   static bool done[128] = {};
   constexpr int bytes = Smem<KV>::kDynamic;
   const cudaError_t e = once_per_device(mu, done, [] {
-    return cudaFuncSetAttribute(score_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return cudaFuncSetAttribute(score_kernel<KV, kBatched>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   });
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -691,15 +869,19 @@ cudaError_t launch_kv(const CUtensorMap &kmap, const ScoreArgs &a, int num_ctas,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_kernel<KV>, kmap, a);
+  return cudaLaunchKernelEx(&cfg, score_kernel<KV, kBatched>, kmap, a);
 }
 
 }  // namespace
 
-cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, int num_ctas,
+cudaError_t launch_score(const CUtensorMap &kmap, const ScoreArgs &a, int kv_dtype, bool batched, int num_ctas,
                          cudaStream_t stream) {
-  if (kv_dtype == IDX_KV_E4M3) return launch_kv<IDX_KV_E4M3>(kmap, a, num_ctas, stream);
-  return launch_kv<IDX_KV_BF16>(kmap, a, num_ctas, stream);
+  if (kv_dtype == IDX_KV_E4M3) {
+    return batched ? launch_kv<IDX_KV_E4M3, true>(kmap, a, num_ctas, stream)
+                   : launch_kv<IDX_KV_E4M3, false>(kmap, a, num_ctas, stream);
+  }
+  return batched ? launch_kv<IDX_KV_BF16, true>(kmap, a, num_ctas, stream)
+                 : launch_kv<IDX_KV_BF16, false>(kmap, a, num_ctas, stream);
 }
 
 }  // namespace idx

@@ -59,7 +59,7 @@ def test_workspace_size_and_validation(idxlib):
     assert idxlib.workspace_size(p, 2049) == 0
     assert idxlib.workspace_size(p, 0) == 0
     bad = [dict(q=None), dict(R=0), dict(max_bound=64 * 64 + 1), dict(kv_dtype=7), dict(k_scale=None),
-           dict(kv_dtype=idxlib.IDX_KV_BF16), dict(q=0x10008), dict(P=0), dict(pt_stride=0)]
+           dict(kv_dtype=idxlib.IDX_KV_BF16), dict(q=0x10008), dict(P=0), dict(pt_stride=0), dict(rows_hint=-1)]
     for kw in bad:
         assert idxlib.workspace_size(_fake_problem(idxlib, **kw), 2048) == 0, kw
     ok_bf16 = _fake_problem(idxlib, kv_dtype=idxlib.IDX_KV_BF16, k_scale=None)

@@ -178,6 +178,63 @@ def test_bad_page_id_is_reported(lib, orc):
     assert st == lib.IDX_OK
 
 
+HINT_CASES = [
+    # name, lengths, rows per request, kv, extra build args
+    ("lone_rows_e4m3", [20000, 9000, 300, 64], [1, 1, 1, 1], "e4m3", {}),
+    ("row_pairs_e4m3", [12000, 700, 5000], [2, 2, 1], "e4m3", {"key_dist": "mixture", "dup_frac": 0.02}),
+    ("row_pairs_bf16", [9000, 4097], [2, 1], "bf16", {}),
+    ("mixed_rows_e4m3", [6000, 3000, 2000, 129], [4, 1, 3, 2], "e4m3", {}),
+    ("negative_scales", [3000, 1000], [1, 2], "e4m3", {"negate_every": 3}),
+]
+
+
+@pytest.mark.parametrize("name,lengths,rows,kv,extra", HINT_CASES, ids=[c[0] for c in HINT_CASES])
+def test_rows_hint_never_changes_the_result(lib, orc, name, lengths, rows, kv, extra):
+    """idx_problem.rows_hint picks the scan: 1 or 2 the batched one (several tiles
+    per accumulator, every epilogue warp busy), anything else the plain one.
+    Scores, fused histogram and selection must be identical for every hint, also
+    for hints below the true row count, and match the oracle."""
+    extra = dict(extra)
+    negate = extra.pop("negate_every", 0)
+    prob = workloads.build(name, lengths, rows, kv, seed=zlib.crc32(name.encode()) % 1000, **extra)
+    if negate:
+        prob.k_scale[::negate] *= -1.0
+    got = {}
+    for hint in (0, 1, 2, 4):
+        dp = lib.DeviceProblem(prob, rows_hint=hint)
+        scores, hist = dp.score()
+        out = dp.launch()
+        assert dp.status() == lib.IDX_OK, hint
+        got[hint] = (scores.cpu().numpy(), hist.cpu().numpy().view(np.uint32), out.cpu().numpy())
+    s0, h0, o0 = got[0]
+    gpu_util.check_scores_vs_oracle(orc, prob, s0, h0)
+    gpu_util.check_selection(orc, o0, s0, prob.row_bound, prob.K)
+    for hint, (s, h, o) in got.items():
+        for r in range(prob.R):
+            b = int(prob.row_bound[r])
+            assert np.array_equal(s[r, :b], s0[r, :b]), (hint, r)
+        assert np.array_equal(h, h0), hint
+        assert np.array_equal(o, o0), hint
+
+
+def test_wait_limit_in_the_batched_scan(lib, orc):
+    """The batched scan (a lone row, hint 1) held back at its first hand-off also
+    ends in IDX_ETIMEOUT and leaves the context usable."""
+    prob = workloads.build("stall_lone", [6000], [1], "e4m3", seed=15)
+    dp = lib.DeviceProblem(prob, rows_hint=1)
+    prev = lib.debug_set(lib.IDX_DEBUG_WAIT_LIMIT_NS, 20_000_000)
+    try:
+        lib.debug_set(lib.IDX_DEBUG_STALL_SCORE_MMA, 1)
+        dp.score()
+        assert dp.status() == lib.IDX_ETIMEOUT
+    finally:
+        lib.debug_set(lib.IDX_DEBUG_STALL_SCORE_MMA, 0)
+        lib.debug_set(lib.IDX_DEBUG_WAIT_LIMIT_NS, prev)
+    scores, hist = dp.score()
+    assert dp.status() == lib.IDX_OK
+    gpu_util.check_scores_vs_oracle(orc, prob, scores.cpu().numpy(), hist.cpu().numpy().view(np.uint32))
+
+
 def test_wait_limit_reports_timeout_and_context_survives(lib, orc):
     """A scoring launch told to hold back its first accumulator hand-off: the
     epilogue's wait runs out (limit 20 ms), the kernel records IDX_ETIMEOUT and
