@@ -170,6 +170,8 @@ size_t idx_host_arena_size(const idx_problem *host_problem, int32_t K);
 
 /* idx_launch on HOST inputs.  host_problem's array pointers are host memory (pinned
  * memory makes the copies asynchronous; pageable memory makes them synchronous).
+ * A rows_hint of 0 is replaced by the most rows of any request, counted from the
+ * host row map.
  * Copies every input into `arena` (device, arena_bytes >= idx_host_arena_size()),
  * runs idx_launch and copies the [R][K] result back into host_out (host).  All
  * copies are issued on `stream`; the caller synchronises the stream before reading

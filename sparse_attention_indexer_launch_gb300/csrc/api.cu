@@ -4,11 +4,13 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <climits>
 #include <mutex>
+#include <vector>
 
 #include "idx.h"
 #include "idx_device.cuh"
@@ -427,6 +429,15 @@ idx_status idx_launch_host(const idx_problem *hp, int32_t K, int32_t *host_out, 
     if (st != IDX_OK) return st;
   }
   idx_problem dp = *hp;
+  if (dp.rows_hint == 0) {   // the row map is host memory here: count each request's rows
+    std::vector<int32_t> rows(static_cast<size_t>(hp->Q), 0);
+    int32_t most = 0;
+    for (int32_t r = 0; r < hp->R; ++r) {
+      const int32_t q = hp->row_req[r];
+      if (q >= 0 && q < hp->Q) most = std::max(most, ++rows[static_cast<size_t>(q)]);
+    }
+    dp.rows_hint = most;
+  }
   dp.q = b + A.q;
   dp.w = reinterpret_cast<const float *>(b + A.w);
   dp.k_cache = b + A.kc;

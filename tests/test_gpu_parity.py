@@ -254,8 +254,11 @@ def test_wait_limit_reports_timeout_and_context_survives(lib, orc):
     gpu_util.check_scores_vs_oracle(orc, prob, scores, hist)
 
 
-def test_launch_from_host_buffers(lib, orc):
-    prob = workloads.build("host", [3000, 700], [4, 1], "e4m3", seed=15)
+@pytest.mark.parametrize("lengths,rows", [([3000, 700], [4, 1]), ([5000, 900], [1, 1])], ids=["rows4", "lone_rows"])
+def test_launch_from_host_buffers(lib, orc, lengths, rows):
+    """idx_launch_host (hint 0: the library counts the rows per request from the
+    host row map, so lone rows take the batched scan) equal to idx_launch."""
+    prob = workloads.build("host", lengths, rows, "e4m3", seed=15)
     host = {k: torch.from_numpy(getattr(prob, k)).pin_memory()
             for k in ("q", "w", "k_cache", "k_scale", "page_table", "row_req", "row_bound")}
     hp = lib.make_problem(host["q"], host["w"], host["k_cache"], host["k_scale"], host["page_table"],
