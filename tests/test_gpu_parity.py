@@ -39,6 +39,9 @@ SMALL = [
     # more rows than one block of the planning pass: the plan's group records go
     # through global memory between its two passes
     ("rows_over_1024", [(i * 53) % 600 + 1 for i in range(280)], [4] * 280, "e4m3", {}),
+    # one long request among many short ones: most CTAs of the rows x slices
+    # selection grid find their slice past the row's end
+    ("long_among_short", [60000] + [(i * 37) % 2000 + 1 for i in range(99)], [2] * 100, "e4m3", {}),
 ]
 
 
