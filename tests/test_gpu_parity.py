@@ -145,11 +145,9 @@ def test_topk_given_adversarial_scores(lib, orc):
         gpu_util.check_selection(orc, out.cpu().numpy(), s, bounds, K)
 
 
-@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4, "3b"])
-def test_configs_full_size(lib, orc, cfg):
-    """The five workloads at full size: sampled scores, the fused histogram, exact
-    selection on the GPU's scores, and the end-to-end rule against the oracle."""
-    prob = workloads.make_config(cfg)
+def _check_whole_problem(lib, orc, prob, label):
+    """Every visible score against the oracle, the fused histogram, exact selection
+    on the GPU's scores (idx_topk and the fused launch), and the end-to-end rule."""
     dp, scores, hist, st = gpu_util.run_score(lib, prob)
     assert st == lib.IDX_OK, lib.status_string(st)
     R, b = prob.R, prob.row_bound
@@ -167,7 +165,30 @@ def test_configs_full_size(lib, orc, cfg):
     assert worst <= 1.0, (worst, where)
     O = orc.topk(ref.astype(np.float32), b, prob.K)
     swaps = parity.check_endtoend(launch, ref, O, b, prob.K)
-    print(f"cfg{cfg}: worst score error {worst:.3f} of tolerance, {swaps} allowed swaps")
+    print(f"{label}: worst score error {worst:.3f} of tolerance, {swaps} allowed swaps")
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4, "3b"])
+def test_configs_full_size(lib, orc, cfg):
+    """The five workloads at full size, in the launch configuration the benchmark
+    times."""
+    _check_whole_problem(lib, orc, workloads.make_config(cfg), f"cfg{cfg}")
+
+
+LARGEST = [
+    # 8,192 rows (2,048 requests of four): the plan's passes over many row blocks,
+    # the selection over thousands of short rows
+    ("rows_8192", [(i * 131) % 300 + 1 for i in range(2048)], [4] * 2048, "e4m3", {}),
+    # a request of 1,572,864 keys (24,576 pages) read by a row and its neighbour
+    ("keys_1_5m", [1_572_864], [2], "e4m3", {"key_dist": "mixture"}),
+]
+
+
+@pytest.mark.parametrize("name,lengths,rows,kv,extra", LARGEST, ids=[c[0] for c in LARGEST])
+def test_largest_shapes(lib, orc, name, lengths, rows, kv, extra):
+    """Shapes well past the benchmark's: many more rows, three times the keys."""
+    prob = workloads.build(name, lengths, rows, kv, seed=zlib.crc32(name.encode()) % 1000, **extra)
+    _check_whole_problem(lib, orc, prob, name)
 
 
 def test_bad_page_id_is_reported(lib, orc):
