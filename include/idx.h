@@ -1,12 +1,11 @@
 /*
  * idx.h - C ABI of the GB300 decode indexer library (libidx.so).
  *
- * The indexer of the sglang PR 48224 page (sgl-amd-mono #86, "... first digits
- * from the scoring"): for every decode row it "scores every cached key of each
- * row and then selects each row's exact top-2048" (section Motivation, first
- * paragraph), reading an FP8 E4M3 or bf16 paged key cache (section Accuracy
- * Tests), dropping "keys at or past a row's bound" (section Modifications,
- * commit 2), and selecting by radix digits whose first digit is radix_key >> 26
+ * The indexer of the sglang PR 48224 page (sgl-amd-mono #86): every decode row is
+ * scored against every key its request has cached, and the row's exact top-2048
+ * is selected (section Motivation, first paragraph).  It reads an FP8 E4M3 or
+ * bf16 paged key cache (section Accuracy Tests), leaves out positions from a
+ * row's bound on (section Modifications, commit 2), and selects by radix digits whose first digit is radix_key >> 26
  * over 64 bins (section Modifications, commit 4).  The score of the key at
  * logical position t for row r is
  *

@@ -8,7 +8,7 @@ gcc into ``_build/liboracle.so`` and marshals numpy arrays to it.
 
 What it computes is the method of the sglang PR 48224 page (sgl-amd-mono #86):
 every cached key of each row scored (section Motivation, first paragraph),
-keys at or past a row's bound dropped (section Modifications, commit 2), each
+positions from a row's bound on left out (section Modifications, commit 2), each
 row's exact top-2048 selected (section Motivation; section Accuracy Tests), and
 the first radix digit ``radix_key >> 26`` over 64 bins (section Modifications,
 commit 4).  The score formula is sum_h w_h * ReLU(scale * <q_h, k>) over 64
@@ -121,7 +121,7 @@ class Oracle:
         return np.array([f(int(b)) for b in bits.ravel()], dtype=np.float64).reshape(bits.shape)
 
     def score(self, prob, ld: int | None = None) -> np.ndarray:
-        """Double-precision scores [R][ld]; positions at or past a row's bound are NaN."""
+        """Double-precision scores [R][ld]; positions from a row's bound on are NaN."""
         kv, kc, ks = _kv(prob)
         q = _c(prob.q, np.uint16)
         w = _c(prob.w, np.float32)

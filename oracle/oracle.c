@@ -6,17 +6,15 @@
  * and the benchmark's CPU-baseline leg may load it.  It shares no code, header,
  * table or constant with the CUDA library; neither side includes the other.
  *
- * Source of the method: the sglang PR 48224 page (squashed sgl-amd-mono #86,
- * "... keys straight into registers, the scoring layout ahead, first digits from
- * the scoring"):
- *   - "scores every cached key of each row and then selects each row's exact
- *     top-2048"                                        (section Motivation, first paragraph)
+ * Source of the method: the sglang PR 48224 page (squashed sgl-amd-mono #86):
+ *   - each row scored against every key its request has cached, then the row's
+ *     exact top-2048 selected                          (section Motivation, first paragraph)
  *   - FP8 E4M3 and bf16 key caches                    (section Accuracy Tests)
- *   - keys at or past a row's bound are dropped       (section Modifications, commit 2)
+ *   - positions from a row's bound on are not scored  (section Modifications, commit 2)
  *   - first radix digit is radix_key >> 26, 64 bins   (section Modifications, commit 4)
  * The score formula itself, score(s) = sum_h w_h * ReLU(scale_s * <q_h, k_s>) over
  * 64 heads of 128 dims, is the indexer statement the build is scoped by; the page
- * only names its "head-half reduction" (section Motivation, first bullet).
+ * only names a reduction over halves of the heads (section Motivation, first bullet).
  *
  * All arithmetic is in IEEE double.  Each function is the definition written out;
  * nothing is blocked or fused beyond what the definition states.

@@ -2,8 +2,7 @@
 //
 // "Release Test Suite - GLM-5.2-EXL3" page, section Config change: decode
 // context parallelism shards a request's KV cache over GPUs and merges the
-// indexer's top-k at an owner ("top-k owner merge"; "exact DCP top-k owner
-// exchange").  Each shard selects its own top-K of the keys it holds, with their
+// indexer's top-k at an owner GPU, by an exchange the page calls exact.  Each shard selects its own top-K of the keys it holds, with their
 // scores; the global top-K is a subset of the union of the shards' lists (a key
 // that is not in its own shard's top-K has K keys above it), so merging the
 // lists by the same order gives the unsharded selection exactly.

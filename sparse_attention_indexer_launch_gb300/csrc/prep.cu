@@ -3,8 +3,8 @@
 // One launch, R + 1 blocks.  Blocks 0..R-1 each prepare one row's query as the B
 // operand of the tensor-core contraction and clear that row's selection state;
 // block R plans the scoring layout (row groups and their tiles).  This is the
-// GB300 counterpart of the sglang PR 48224 page's "scoring layout ahead"
-// (section Modifications, commit 3): the row groups, their requests and each
+// GB300 counterpart of the sglang PR 48224 page's scoring layout computed in
+// advance (section Modifications, commit 3): the row groups, their requests and each
 // row's index bound are worked out once, on the device, before the scan.
 #include <cuda_fp8.h>
 

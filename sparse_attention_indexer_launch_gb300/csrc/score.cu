@@ -2,10 +2,10 @@
 // (tcgen05, accumulator in TMEM), the ReLU-weighted head reduction, the score
 // store and the fused score histogram.
 //
-// sglang PR 48224 page (sgl-amd-mono #86): "scores every cached key of each row"
-// (section Motivation, first paragraph); rows of one request read each key once
-// (section Modifications, commit 1); the store drops "keys at or past a row's
-// bound" (commit 2); the first radix digit radix_key >> 26 of every stored score
+// sglang PR 48224 page (sgl-amd-mono #86): each row is scored against every key
+// its request has cached (section Motivation, first paragraph); rows of one
+// request read each key once (section Modifications, commit 1); positions from a
+// row's bound on are not stored (commit 2); the first radix digit radix_key >> 26 of every stored score
 // is counted in 64 bins per row during the scan, so the selection needs no pass
 // of its own for it (commit 4, the score_hist mailbox).  Here the scan counts the
 // top 12 bits of the radix key; the first digit's 64 bins are its marginal.

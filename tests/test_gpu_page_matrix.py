@@ -3,8 +3,8 @@ through the C ABI, against the oracle.
 
 sglang PR 48224 page, section Accuracy Tests: the top-k check runs at positions
 8447, 131071, 262143 and 524287 (bound = position + 1) with 2, 4 and 8 rows of
-one request; the 2-row case is a request and its pad row (section
-Modifications, commit 1: "a request and its pad row"), the 8-row case the draft
+one request; the 2-row case is a live row with a pad row of the same request
+(section Modifications, commit 1), the 8-row case the draft
 chain of two groups of four.  Every visible score is compared with the oracle
 within |err| <= 1e-3 + 2e-3 |ref|, the fused first-digit histogram exactly, the
 selection bit-exactly on the GPU's own scores, the fused launch against that
