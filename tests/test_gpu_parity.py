@@ -293,3 +293,29 @@ def test_launch_from_host_buffers(lib, orc, lengths, rows):
     torch.cuda.synchronize()
     dp = lib.DeviceProblem(prob)
     assert np.array_equal(out.numpy(), dp.launch().cpu().numpy())
+
+
+def test_launch_replays_from_a_cuda_graph(lib, orc):
+    """idx_launch captured into a CUDA graph (its four kernels and their
+    programmatic dependencies) replays to the direct call's result, twice in a row,
+    and its status word reads clean."""
+    prob = workloads.build("graph", [7000, 3000], [4, 1], "e4m3", seed=16)
+    dp = lib.DeviceProblem(prob)
+    want = dp.launch().cpu().numpy()
+    out = torch.full((prob.R, prob.K), -5, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        dp.launch(out, stream=side)       # one-time setup happens outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    out.fill_(-5)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dp.launch(out, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        out.fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), want)
+    assert dp.status() == lib.IDX_OK
