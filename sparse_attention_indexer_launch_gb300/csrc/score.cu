@@ -29,6 +29,9 @@
 //               shape so that each thread needs only 16 of the row's weights
 //               (held in registers), and hands the accumulator back right after
 //               its last TMEM read.
+// The batched instance (kBatched, for launches whose requests have one or two
+// rows: a lone live row and its pad row) fills each accumulator with 4 / rows
+// tiles of a group and gives every epilogue warp one (tile, row) of the batch.
 // E4M3 cache: keys feed tcgen05.mma kind::f8f6f4 straight from the TMA ring; the
 // query is split exactly into two E4M3 terms (prep.cu), run as K = 2 x 128.
 // bf16 cache: keys and query are bf16, kind::f16, K = 128.
