@@ -319,3 +319,39 @@ def test_launch_replays_from_a_cuda_graph(lib, orc):
         torch.cuda.synchronize()
         assert np.array_equal(out.cpu().numpy(), want)
     assert dp.status() == lib.IDX_OK
+
+
+def test_concurrent_launches_on_two_streams(lib, orc):
+    """Two problems with their own workspaces, launched back to back on two
+    streams so that their kernels can overlap, give the results each gives alone
+    (the library keeps no state of a launch outside the caller's workspace)."""
+    pa = workloads.build("stream_a", [9000, 4000], [4, 2], "e4m3", seed=17)
+    pb = workloads.build("stream_b", [12000], [1], "bf16", seed=18)
+    da, db = lib.DeviceProblem(pa), lib.DeviceProblem(pb)
+    want_a, want_b = da.launch().cpu().numpy(), db.launch().cpu().numpy()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    oa = torch.empty((pa.R, pa.K), dtype=torch.int32, device="cuda")
+    ob = torch.empty((pb.R, pb.K), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(3):
+        oa.fill_(-9)
+        ob.fill_(-9)
+        torch.cuda.synchronize()
+        da.launch(oa, stream=sa)
+        db.launch(ob, stream=sb)
+        torch.cuda.synchronize()
+        assert np.array_equal(oa.cpu().numpy(), want_a)
+        assert np.array_equal(ob.cpu().numpy(), want_b)
+    assert da.status(sa) == lib.IDX_OK and db.status(sb) == lib.IDX_OK
+
+
+@pytest.mark.parametrize("K", [1, 100, 2047])
+def test_launch_at_other_k(lib, orc, K):
+    """The fused launch at K other than 2048, against the oracle's selection of
+    the same K on the GPU's own scores."""
+    prob = workloads.build("other_k", [5000, 1500, 90], [4, 2, 1], "e4m3", seed=19)
+    dp = lib.DeviceProblem(prob, K=K)
+    scores, _ = dp.score()
+    out = dp.launch().cpu().numpy()
+    assert out.shape == (prob.R, K) and dp.status() == lib.IDX_OK
+    gpu_util.check_selection(orc, out, scores.cpu().numpy(), prob.row_bound, K)
