@@ -50,8 +50,10 @@ constexpr int kThreads = 512;              // hist12 and finish
 constexpr int kSortCap = IDX_MAX_K;        // power of two
 constexpr int kTilesPerWarp = kSortCap / 64 / (kThreads / 32);   // 64-key sort tiles per warp
 constexpr int kFinishSmem = (kTieCap + kSortCap) * 8 + 2 * 4096 * 4;   // candidates, the keys to sort, buckets
-// Requested by each finish CTA: more than half an SM's shared memory, so that the
-// scheduler gives every CTA an SM of its own instead of packing two on one.
+// Requested by each finish CTA while the grid has no more CTAs than the device has
+// SMs: more than half an SM's shared memory, so that the scheduler gives every CTA
+// an SM of its own instead of packing two on one.  Larger grids ask for what the
+// kernel uses, so that two CTAs share an SM and the grid needs fewer waves.
 constexpr int kFinishSmemAlloc = 120 * 1024;
 static_assert(kFinishSmem <= kFinishSmemAlloc, "finish shared memory");
 constexpr uint32_t kNoBin = 0xFFFFFFFFu;
@@ -876,7 +878,7 @@ cudaError_t launch_collect(const SelectArgs &a_in, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   cfg.gridDim = dim3(2, a.R);   // per row: the winners' CTA and the candidates' CTA
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kFinishSmemAlloc;
+  cfg.dynamicSmemBytes = 2 * a.R > a.num_sms ? kFinishSmem : kFinishSmemAlloc;
   return cudaLaunchKernelEx(&cfg, finish_kernel, a);
 }
 
