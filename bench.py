@@ -413,6 +413,61 @@ def roofline_terms(prob, hbm_gbs, bf16_tf):
     return max(t_hbm, t_fp8), ("hbm" if t_hbm >= t_fp8 else "tensor"), fp8_tf
 
 
+def run_split(args):
+    """--op split: the indexer's two halves called apart on the benchmark workload,
+    idx_score (prep and the scan, scores and first digit out) and idx_topk on those
+    scores (its own 12-bit histogram pass, collect, finish), each timed like the
+    fused launch (L2 flushed before every call, CUDA events around it).  The sum
+    against idx_launch shows what fusing the histogram into the scan saves."""
+    import numpy as np
+    import torch
+    import oracle
+    import sparse_attention_indexer_launch_gb300 as lib
+    import workloads
+    orc = oracle.default()
+    prob = workloads.make_config(3)
+    dp = lib.DeviceProblem(prob)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    scores, hist = dp.score()
+    out = torch.empty((prob.R, prob.K), dtype=torch.int32, device="cuda")
+    ld = scores.shape[1]
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+
+    # preallocated outputs: nothing but the library's kernels between the events
+    score_us = timed(lambda: lib.idx_score(dp.problem, scores, ld, hist, dp.ws))
+    topk_us = timed(lambda: lib.idx_topk(scores, ld, dp.row_bound, prob.R, dp.max_bound, prob.K, None, out,
+                                         dp.ws))
+    launch_us = timed(lambda: lib.idx_launch(dp.problem, prob.K, out, dp.ws))
+    got = dp.topk(scores).cpu().numpy()
+    if not np.array_equal(got, orc.topk(scores.cpu().numpy(), prob.row_bound, prob.K)):
+        raise SystemExit("idx_topk differs from the oracle's selection on the same scores")
+    if dp.status() != lib.IDX_OK:
+        raise SystemExit("device status not clean")
+    key_rows = int(prob.row_bound.astype(np.int64).sum())
+    print(json.dumps({"metric": "µs per idx_score and per idx_topk on the benchmark workload", "op": "split",
+                      "value": score_us + topk_us, "unit": "µs", "higher_is_better": False, "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "idx_score_us": score_us,
+                      "idx_topk_us": topk_us, "idx_launch_us": launch_us,
+                      "topk_key_rows_per_s": key_rows / (topk_us * 1e-6),
+                      "config": {"workload": "cfg3: 2 requests x 4 rows, 524,288 keys each, E4M3",
+                                 "l2": "flushed before every call (256 MB write)"}}))
+    return 0
+
+
 def run_merge(args):
     """--op merge: idx_merge_topk of S ranked parts of R rows x K (the key-sharded
     indexer's owner merge), S = 2, 4, 8; CUDA events around each call, L2 flushed
@@ -479,9 +534,10 @@ def main():
                          "extra_configs; 'none' for none")
     ap.add_argument("--ref-budget", type=float, default=120.0,
                     help="seconds for the whole --impl reference run")
-    ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch", "merge"],
+    ap.add_argument("--op", default="indexer", choices=["indexer", "top1", "patch", "merge", "split"],
                     help="indexer: the fused indexer launch (the benchmark); top1: the one-launch top-1; "
-                         "patch: the new-key patch; merge: the key-sharded owner merge")
+                         "patch: the new-key patch; merge: the key-sharded owner merge; "
+                         "split: idx_score and idx_topk called apart")
     ap.add_argument("--top1-rows", type=int, default=8)
     ap.add_argument("--top1-vocab", type=int, default=151552)
     args = ap.parse_args()
@@ -494,6 +550,8 @@ def main():
         return run_top1(args)
     if args.op == "patch":
         return run_patch(args)
+    if args.op == "split":
+        return run_split(args)
     if args.op == "merge":
         return run_merge(args)
 

@@ -163,9 +163,19 @@ __global__ void __launch_bounds__(kThreads) hist12_kernel(const SelectArgs a) {
   for (int i = threadIdx.x; i < kHistBins; i += kThreads) h[i] = 0u;
   __syncthreads();
   const int64_t begin = static_cast<int64_t>(blockIdx.x) * kSlice;
-  const int64_t end = min(static_cast<int64_t>(B), begin + kSlice);
-  const float *row = a.scores + static_cast<int64_t>(r) * a.ld;
-  for (int64_t pos = begin + threadIdx.x; pos < end; pos += kThreads) atomicAdd(&h[radix_key(row[pos]) >> 20], 1u);
+  const int n = static_cast<int>(min(static_cast<int64_t>(B), begin + kSlice) - begin);
+  const float *row = a.scores + static_cast<int64_t>(r) * a.ld + begin;
+  // every load of the thread goes out before any is counted
+  constexpr int kPer = kSlice / kThreads;
+  float x[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int j = i * kThreads + threadIdx.x;
+    x[i] = j < n ? __ldcs(row + j) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (i * kThreads + static_cast<int>(threadIdx.x) < n) atomicAdd(&h[radix_key(x[i]) >> 20], 1u);
   __syncthreads();
   for (int i = threadIdx.x; i < kHistBins; i += kThreads)
     if (h[i]) atomicAdd(&a.ws.hist12[static_cast<int64_t>(r) * kHistBins + i], h[i]);
