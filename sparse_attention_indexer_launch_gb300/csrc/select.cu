@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t scratch[36];
   __shared__ uint32_t nwin, ncand;
+  __shared__ uint32_t wbase_s, cbase_s;
   __shared__ int abort_flag;
 
   grid_dependency_wait();   // scores and histogram come from the previous launch
@@ -351,9 +352,18 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
     uint32_t tot;
     const uint32_t ex = block_excl_scan((cw << 16) | cc, scratch, &tot);
     uint32_t wpos = ex >> 16, cpos = ex & 0xFFFFu;
+    // One thread reserves both runs on the row's lists (two atomics in flight
+    // together); their round trip runs under pass 2.  More candidates than one
+    // slice keeps: the finish resolves the row from its scores.
+    uint32_t wb = 0u, cb = 0u;
     if (tid == 0) {
+      const uint32_t nw0 = min(tot >> 16, static_cast<uint32_t>(kWinList)), nc0 = tot & 0xFFFFu;
       nwin = tot >> 16;
-      ncand = tot & 0xFFFFu;
+      ncand = nc0;
+      wb = nw0 > 0u ? atomicAdd(&ws.rowsel[r].win_count, nw0) : 0u;
+      cb = nc0 > 0u ? atomicAdd(&ws.rowsel[r].tie_count, nc0 <= static_cast<uint32_t>(kCandList)
+                                                          ? nc0 : static_cast<uint32_t>(kTieCap) + 1u)
+                    : 0u;
     }
     // pass 2: the marked quads again, writing the keys' offsets within the slice
     while (qmask) {
@@ -374,23 +384,16 @@ __global__ void __launch_bounds__(kCollectThreads) collect_kernel(const SelectAr
         }
       }
     }
+    if (tid == 0) {
+      wbase_s = wb;
+      cbase_s = cb;
+    }
   }
   __syncthreads();
 
-  // 4. winners onto the row's winner list; candidates onto its candidate list.
-  //    One thread reserves both ranges (two atomics in flight together).
+  // 4. winners onto the row's winner list; candidates onto its candidate list
   const uint32_t nw = min(nwin, static_cast<uint32_t>(kWinList));
   const uint32_t nc = ncand;
-  RowSelect &rs = ws.rowsel[r];
-  __shared__ uint32_t wbase_s, cbase_s;
-  if (tid == 0) {
-    wbase_s = nw > 0u ? atomicAdd(&rs.win_count, nw) : 0u;
-    // more candidates than one slice keeps: the finish resolves the row from its scores
-    cbase_s = nc > 0u ? atomicAdd(&rs.tie_count, nc <= static_cast<uint32_t>(kCandList)
-                                                     ? nc : static_cast<uint32_t>(kTieCap) + 1u)
-                      : 0u;
-  }
-  __syncthreads();
   unsigned long long *win = ws.win + static_cast<int64_t>(r) * a.K;
   for (uint32_t i = tid; i < nw; i += kCollectThreads) {
     const uint32_t slot = wbase_s + i;
