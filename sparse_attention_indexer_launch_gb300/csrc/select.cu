@@ -702,11 +702,23 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
 
   if (part == 0) {
     // The winners (keys above T, fewer than K) are the first output slots: one
-    // bucket sort of the row's whole winner list.
+    // bucket sort of the row's whole winner list.  The list is read whole together
+    // with its length (one round trip, not two); entries past the length are unused.
+    const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
+    constexpr int kPer = IDX_MAX_K / kThreads;
+    unsigned long long wv[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int i = m * kThreads + tid;
+      wv[m] = i < K ? __ldcg(&win[i]) : 0ull;
+    }
     const uint32_t nw = min(__ldcg(&rs.win_count), static_cast<uint32_t>(nout));
     if (nw == 0u) return;
-    const unsigned long long *win = ws.win + static_cast<int64_t>(r) * K;
-    for (uint32_t i = tid; i < nw; i += kThreads) sel[i] = __ldcg(&win[i]);
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const uint32_t i = static_cast<uint32_t>(m * kThreads + tid);
+      if (i < nw) sel[i] = wv[m];
+    }
     __syncthreads();
     const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, static_cast<int>(nw), bstart, bcur, scratch);
     for (uint32_t i = tid; i < nw; i += kThreads)
