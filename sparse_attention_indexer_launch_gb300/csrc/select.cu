@@ -532,13 +532,15 @@ __device__ __forceinline__ int sort_size(int n);
 // A key's rank costs one compare per member of its group, so groups of up to
 // kGroupMax keys are ranked this way; when some group holds more (many equal or
 // near-equal scores) the segment is sorted by block_sort_desc instead.  tmp[] (kSortCap keys)
-// and start[], cur[] (4096 words each) are scratch.  Returns the buffer holding
-// the result.  Every thread of the block must call.
+// and start[], cur[] (4096 words each) are scratch.  Each key leaves through
+// emit(slot, key) with its slot in the descending order, from whichever thread
+// ranked it.  Every thread of the block must call.
 constexpr int kBuckets = 4096;
 constexpr int kGroupMax = 256;
 
-__device__ unsigned long long *block_bucket_sort_desc(unsigned long long *s, unsigned long long *tmp, int n,
-                                                      uint32_t *start, uint32_t *cur, uint32_t *scratch) {
+template <typename Emit>
+__device__ void block_bucket_sort_desc(unsigned long long *s, unsigned long long *tmp, int n, uint32_t *start,
+                                       uint32_t *cur, uint32_t *scratch, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // 1. range of the 32-bit score keys
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -595,7 +597,9 @@ __device__ unsigned long long *block_bucket_sort_desc(unsigned long long *s, uns
     const int p2 = sort_size(n);
     for (int i = n + tid; i < p2; i += kThreads) s[i] = 0ull;
     __syncthreads();
-    return block_sort_desc(s, tmp, p2);
+    const unsigned long long *sorted = block_sort_desc(s, tmp, p2);
+    for (int i = tid; i < n; i += kThreads) emit(i, sorted[i]);
+    return;
   }
   // 4. each key into its group (arbitrary order within the group)
   for (int i = tid; i < n; i += kThreads) {
@@ -611,10 +615,8 @@ __device__ unsigned long long *block_bucket_sort_desc(unsigned long long *s, uns
     const uint32_t g0 = start[b], g1 = start[b] + cur[b];
     uint32_t r = 0u;
     for (uint32_t j = g0; j < g1; ++j) r += tmp[j] > x ? 1u : 0u;
-    s[g0 + r] = x;
+    emit(static_cast<int>(g0 + r), x);   // the key's final slot, straight out
   }
-  __syncthreads();
-  return s;
 }
 
 __device__ __forceinline__ int sort_size(int n) {
@@ -720,9 +722,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
       if (i < nw) sel[i] = wv[m];
     }
     __syncthreads();
-    const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, static_cast<int>(nw), bstart, bcur, scratch);
-    for (uint32_t i = tid; i < nw; i += kThreads)
-      put(a, static_cast<int64_t>(r) * K + i, sorted[i]);
+    block_bucket_sort_desc(sel, cand, static_cast<int>(nw), bstart, bcur, scratch,
+                           [&](int slot, unsigned long long x) { put(a, static_cast<int64_t>(r) * K + slot, x); });
     return;
   }
 
@@ -846,9 +847,9 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const SelectArgs a) {
   }
   __syncthreads();
   const int n = min(static_cast<int>(count_s), static_cast<int>(need));
-  const unsigned long long *sorted = block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch);
-  for (int i = tid; i < n; i += kThreads)
-    put(a, static_cast<int64_t>(r) * K + above + i, sorted[i]);
+  block_bucket_sort_desc(sel, cand, n, bstart, bcur, scratch, [&](int slot, unsigned long long x) {
+    put(a, static_cast<int64_t>(r) * K + above + slot, x);
+  });
 }
 
 }  // namespace
