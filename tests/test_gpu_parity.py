@@ -355,3 +355,35 @@ def test_launch_at_other_k(lib, orc, K):
     out = dp.launch().cpu().numpy()
     assert out.shape == (prob.R, K) and dp.status() == lib.IDX_OK
     gpu_util.check_selection(orc, out, scores.cpu().numpy(), prob.row_bound, K)
+
+
+@pytest.mark.parametrize("nreq", [3, 12], ids=["rows12", "rows48"])
+def test_bad_bounds_and_requests_are_reported(lib, orc, nreq):
+    """A row bound past max_bound is clamped to it and a request id outside [0, Q)
+    reads nothing; both are reported as IDX_EDEVICE.  The other rows are scored
+    and selected as usual."""
+    prob = workloads.build("badbound", [900] * nreq, [4] * nreq, "e4m3", seed=20)
+    mb = int(prob.max_bound)
+    bad_bound = prob.row_bound.copy()
+    bad_bound[1] = mb + 50
+    for kind in ("bound", "request"):
+        p = workloads.build("badbound", [900] * nreq, [4] * nreq, "e4m3", seed=20)
+        if kind == "bound":
+            p.row_bound[:] = bad_bound
+        else:
+            p.row_req[2] = p.page_table.shape[0] + 3
+        dp = lib.DeviceProblem(p, max_bound=mb, rows_hint=0)
+        scores, _ = dp.score()
+        assert dp.status() == lib.IDX_EDEVICE, kind
+        out = dp.launch().cpu().numpy()
+        assert dp.status() == lib.IDX_EDEVICE, kind
+        scores = scores.cpu().numpy()
+        ref = p
+        if kind == "bound":
+            ref.row_bound[1] = mb                      # what the library scores: the clamped bound
+        else:
+            ref.row_bound[2] = 0                       # the bad row reads nothing
+            ref.row_req[2] = 0
+            assert (out[2] == -1).all()
+        gpu_util.check_scores_vs_oracle(orc, ref, scores)
+        gpu_util.check_selection(orc, out, scores, ref.row_bound, ref.K)
