@@ -111,3 +111,19 @@ def test_patch_rejects_bad_arguments_without_a_gpu(idxlib):
     assert lib.idx_patch_new_keys(C.byref(prob), 0x80008, None) == idxlib.IDX_EINVAL    # not 16-byte aligned
     bad = _fake_problem(idxlib, R=0)
     assert lib.idx_patch_new_keys(C.byref(bad), 0x80000, None) == idxlib.IDX_EINVAL
+
+
+def test_binding_refuses_to_import_without_the_library(tmp_path):
+    """The binding has no fallback: a copy of the package with no built library
+    raises ImportError on import, naming the missing file."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "sparse_attention_indexer_launch_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "sparse_attention_indexer_launch_gb300", "__init__.py"), pkg / "__init__.py")
+    proc = subprocess.run([sys.executable, "-c", "import sparse_attention_indexer_launch_gb300"],
+                          cwd=str(tmp_path), env={**os.environ, "PYTHONPATH": str(tmp_path)},
+                          capture_output=True, text=True, timeout=120)
+    assert proc.returncode != 0
+    assert "ImportError" in proc.stderr and "libidx.so is not built" in proc.stderr
