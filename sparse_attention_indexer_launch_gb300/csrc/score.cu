@@ -41,7 +41,7 @@
 namespace idx {
 namespace {
 
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 16;                  // the histogram flush deals its blocks for sixteen
 constexpr int kProducers = 2;                  // producer warps for an E4M3 cache
 constexpr int kEpiWarp0 = 2;                            // warps 2 .. 17: the epilogue
 constexpr int kProducer2Warp = kEpiWarp0 + kEpiWarps;   // the second producer, after the epilogue warps
@@ -580,31 +580,34 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // Every row's histogram goes to global memory (12-bit counts, the 64-bin first
     // digit, and the caller's copy of the latter when asked) and is cleared; all
     // sixteen warps meet before and after.  The group's nrows x 64 (row, first digit)
-    // blocks of 64 bins are dealt round-robin to the warps, four at a time: the four
+    // blocks of 64 bins are dealt to the warps, four per row at a time: the four
     // shared-memory reads go out together, and a block with no count (most of them:
     // a CTA's scores fill a few hundred of a row's 4096 bins) costs one vote.  A
     // block with counts is unpacked into one of the warp's staging slots and added
     // to the row's 12-bit histogram by one bulk reduction (the TMA engine performs
-    // the 64 additions); its sum goes to the first digit by one atomic.
+    // the 64 additions); its sum goes to the first digit by one atomic.  The counts
+    // sit in a few first digits, the same ones in every row: scores of magnitude
+    // near 1 fall in digits 15 and 16 (negative) and 47 and 48 (positive).  So warp
+    // w takes the digits d of row r with d + 2 (d >> 5) + 4 r = w (mod 16):
+    // consecutive digits of one sign go to consecutive warps, mirrored digits of the
+    // two signs apart, and each row is shifted by four, which puts those sixteen
+    // blocks on sixteen different warps.
     uint32_t *stage = sflush + ew * (kStageBlocks * 64);
     auto flush = [&]() -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->hdone[0]);
       if (!mbar_wait(&bars->hdone[0], flushes & 1, limit, abort)) return false;
-      const int nblk = grp.nrows * 64;
       int staged = 0;
-      for (int b0 = ew; b0 < nblk; b0 += 4 * kEpiWarps) {
+      for (int hr = 0; hr < grp.nrows; ++hr) {
+        const int x = (ew - 4 * hr) & 15, y = (ew - 4 * hr - 2) & 15;
+        const int ds[4] = {x, x + 16, 32 + y, 48 + y};
         uint32_t wv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int b = b0 + i * kEpiWarps;
-          wv[i] = b < nblk ? shist[(b >> 6) * kHistWords + (b & 63) * 32 + lane] : 0u;
-        }
+        for (int i = 0; i < 4; ++i) wv[i] = shist[hr * kHistWords + ds[i] * 32 + lane];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           if (__ballot_sync(0xffffffffu, wv[i] != 0u) == 0u) continue;   // uniform for the warp
-          const int b = b0 + i * kEpiWarps;
-          const int hr = b >> 6, d = b & 63;
+          const int d = ds[i];
           const int64_t grow = grp.row0 + hr;
           const uint32_t lo = wv[i] & 0xFFFFu, hi = wv[i] >> 16;
           if (staged >= kStageBlocks) {   // the slot's previous block must have been read
