@@ -141,24 +141,19 @@ __device__ __forceinline__ void set_abort(Barriers *bars, uint32_t *status) {
 // Fragment va holds keys lane/4 (registers 4k, 4k+1) and lane/4 + 8 (4k+2,
 // 4k+3), vb the keys 16 lanes further on; repetition k holds heads
 // 8k + 2 (lane % 4) + {0, 1} of the half, whose halved weights are w[k].
-// v + |v| = 2 relu(v) exactly: one FADD on the FMA pipe (|v| is an operand
-// modifier), then a packed FMA per head pair.
+// v + |v| = 2 relu(v) exactly: one packed add per head pair, then a packed FMA
+// per head pair.
 __device__ __forceinline__ void relu_frag(const uint32_t (&va)[16], const uint32_t (&vb)[16], const float2 *w,
                                           float2 (&a)[4]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float e[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float x = __uint_as_float(va[4 * k + i]);
-      const float y = __uint_as_float(vb[4 * k + i]);
-      e[i] = x + fabsf(x);
-      e[4 + i] = y + fabsf(y);
+    for (int j = 0; j < 4; ++j) {   // key j: registers 4k + 2 (j % 2) + {0, 1} of va (j < 2) or vb
+      const uint32_t *v = j < 2 ? va : vb;
+      const float2 x = make_float2(__uint_as_float(v[4 * k + 2 * (j & 1)]), __uint_as_float(v[4 * k + 2 * (j & 1) + 1]));
+      const float2 e = __fadd2_rn(x, make_float2(fabsf(x.x), fabsf(x.y)));
+      a[j] = __ffma2_rn(e, w[k], a[j]);
     }
-    a[0] = __ffma2_rn(make_float2(e[0], e[1]), w[k], a[0]);
-    a[1] = __ffma2_rn(make_float2(e[2], e[3]), w[k], a[1]);
-    a[2] = __ffma2_rn(make_float2(e[4], e[5]), w[k], a[2]);
-    a[3] = __ffma2_rn(make_float2(e[6], e[7]), w[k], a[3]);
   }
 }
 
