@@ -221,11 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     for (int s = 0; s < kScaleSlots; ++s) {
       mbar_init(&bars->sfull[s], 1);           // the producer's arrival; the copies complete by bytes
-      mbar_init(&bars->sempty[s], kEpiWarps);   // every epilogue warp passes every tile
+      // every epilogue thread passes every tile (batched: every warp, for its share)
+      mbar_init(&bars->sempty[s], kBatched ? kEpiWarps : kEpiWarps * 32);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars->tfull[s], kBatched ? kIssuers<KV> : 1);   // batched: every issuer commits every batch
-      mbar_init(&bars->tempty[s], kEpiWarps);   // every epilogue warp reads every tile
+      // every epilogue thread reads every tile (batched: every warp)
+      mbar_init(&bars->tempty[s], kBatched ? kEpiWarps : kEpiWarps * 32);
     }
     mbar_init(&bars->hdone[0], kEpiWarps);
     mbar_init(&bars->hflushed[0], kEpiWarps);
@@ -551,8 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     // weights in registers; the four threads that share keys add their partial
     // sums by shuffles, after which thread `lane` holds key kl of the quarter.
     // The tile's accumulator goes back to the MMA issuer right after the warp's
-    // last TMEM read.  Tile and key indices are 32-bit (a launch has fewer than
-    // 2^31 of either).
+    // last TMEM read; in the plain walk each thread arrives on the slot barriers
+    // itself (no warp sync before a lane-0 arrival).  Tile and key indices are
+    // 32-bit (a launch has fewer than 2^31 of either).
     const int ew = warp - kEpiWarp0;
     const int quarter = warp & 3;            // TMEM lane quarter this warp may read
     const int row = ew >> 2;                 // group row this warp reduces
@@ -791,8 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           break;
         }
         scale = sc[ss * kTileKeys];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->sempty[ss]);
+        mbar_arrive(&bars->sempty[ss]);
       }
       const int slot = k & (kSlots - 1);
       if (!mbar_wait(&bars->tfull[slot], (k / kSlots) & 1, limit, abort)) {
@@ -803,8 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       tc_fence_after();
       if (!mine) {   // the group has no row for this warp: hand the accumulator back at once
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+        mbar_arrive(&bars->tempty[slot]);
         continue;
       }
       const int pos = (t - gbegin) * kTileKeys + qk;
@@ -821,10 +822,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         tmem_wait_ld();
         reg_fence16(va);
         reg_fence16(vb);
-        if (half == 1) {   // every read of this warp is done: hand the accumulator back
+        if (half == 1) {   // every read of this thread is done: hand the accumulator back
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[slot]);
+          mbar_arrive(&bars->tempty[slot]);
         }
         if (negmask == 0u) relu_frag(va, vb, &w2[4 * half], sums);
         else relu_frag_signed(va, vb, &w2[4 * half], (negmask >> (lane & ~3)) & 15u, sums);
