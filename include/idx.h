@@ -23,9 +23,10 @@
  *     argument returns IDX_EINVAL (or IDX_EUNSUPPORTED for a shape the library
  *     does not handle) and launches nothing.  A failed launch returns IDX_ECUDA.
  *   - Errors found on the device (a page id outside [0, P), a row bound above
- *     pt_stride * 64, a pipeline wait that ran out of time) never trap: the kernel
- *     records them in a status word inside the workspace and finishes; read it
- *     with idx_last_device_status().
+ *     max_bound or pt_stride * 64, a request id outside [0, Q), a pipeline wait
+ *     that ran out of time) never trap: the kernel records them in a status word
+ *     inside the workspace, clamps the bound or skips the page or the row, and
+ *     finishes; read the word with idx_last_device_status().
  *   - Key positions are logical positions within the row's request: position t
  *     lives in physical page page_table[req * pt_stride + t / 64], slot t % 64.
  *   - Host threads: any call may be made from several host threads at once, on
