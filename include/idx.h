@@ -58,7 +58,7 @@ typedef enum {
     IDX_EUNSUPPORTED = 2, /* valid but outside what this build handles */
     IDX_ECUDA = 3,        /* a CUDA runtime call or launch failed */
     IDX_ETIMEOUT = 4,     /* a device-side wait ran out of time (device status only) */
-    IDX_EDEVICE = 5       /* bad data seen on the device: page id or bound out of range */
+    IDX_EDEVICE = 5       /* bad data seen on the device: page id, bound or request id out of range */
 } idx_status;
 
 typedef enum {
